@@ -1,0 +1,214 @@
+"""Seeded synthetic decode batches.
+
+This module only draws inputs; it holds none of the attention or assign
+arithmetic, and it is the one piece of Python shared by the CUDA path, the
+oracle-based tests and the benchmark.
+
+The workloads stand in for the pages' mixed-length decode batches (vLLM
+integration post, Table 3 and "The challenge: mixed-length decode in every
+batch"; Hy3's GQA shape of 64 query heads, 8 KV heads, head dim 128 from
+"A Quick Word on Hy3-series models", sliced 8-way for a TP8 GPU).  There is
+no dataset: lengths, page placement and values are drawn from seeds.
+
+Recipe (draw order: seqlens, page permutation, Q, K, V):
+  * seqlens from a CPU torch.Generator seeded with the config's seed;
+    log-uniform lengths are floor(exp(U(ln a, ln b))), uniform ones are
+    integer-uniform on [a, b];
+  * pages: P = sum_r ceil(L_r / 64) physical pages; a random permutation of
+    [0, P) is handed out to the requests in request order; unused
+    block-table entries are -1;
+  * Q ~ N(0, 1) from the same CPU generator;
+  * K, V ~ N(0, 1), drawn on the target device from a generator seeded with
+    seed + 1 (K) and seed + 2 (V); slots past L_r in a request's last page
+    are part of the draw, or are poisoned (NaN / the E4M3 NaN code) on request;
+  * BF16 tensors are the fp32 draws rounded to BF16;
+  * FP8-E4M3: K and V scaled by a per-tensor scale amax / 448, Q by a
+    per-(token, head) scale amax_row / 448, then converted with torch's
+    float8_e4m3fn cast (round to nearest even).  This stands in for the
+    fused prologue that emits FP8 Q and writes the FP8 cache, which lies
+    outside this path.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+HEAD_DIM = 128
+PAGE = 64
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    seqlens: tuple = ()  # explicit lengths, or empty when drawn
+    draw: tuple = ()  # ((count, kind, a, b), ...), kind in {"log", "uniform", "fixed"}
+    kv_dtype: str = "bf16"  # "bf16" or "e4m3"
+    seed: int = 1000
+    num_ctas: int = 0  # 0: one persistent CTA per resident slot on the GPU
+    min_tiles: int = 2
+    description: str = ""
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(HEAD_DIM)
+
+
+WORKLOADS = {
+    "tiny": Workload(
+        "tiny", 4, 8, 1, seqlens=(64, 200, 1000, 2048), seed=1001, num_ctas=132, min_tiles=2,
+        description="tiny BF16 paged GQA decode, B=4, L={64,200,1000,2048}, Hq=8, Hkv=1, "
+                    "132 persistent CTAs, floor 2"),
+    "hy3_tp8": Workload(
+        "hy3_tp8", 32, 8, 1, draw=((32, "log", 1024, 32768),), seed=1002,
+        description="Hy3-shaped TP8 slice, BF16, B=32, Hq=8, Hkv=1, L log-uniform [1K, 32K]"),
+    "skewed": Workload(
+        "skewed", 64, 64, 8, draw=((60, "uniform", 512, 2048), (4, "uniform", 65536, 131072)),
+        seed=1003,
+        description="skewed BF16 TP1 shape, B=64, Hq=64, Hkv=8, 60 x U[512,2K] + 4 x U[64K,128K]"),
+    "uniform": Workload(
+        "uniform", 16, 64, 8, draw=((16, "fixed", 8192, 8192),), seed=1004,
+        description="uniform-length control, BF16, B=16, L=8192, Hq=64, Hkv=8"),
+    "fp8": Workload(
+        "fp8", 64, 8, 1, draw=((64, "log", 1024, 131072),), kv_dtype="e4m3", seed=1005,
+        description="FP8-E4M3 KV and Q, B=64, Hq=8, Hkv=1, L log-uniform [1K, 128K]"),
+}
+
+# The six KV-length mixes of the vLLM post's Table 3 (FP8 decode), at the
+# TP8 head shape.  A x B means A requests at KV length B.
+TABLE3 = {
+    "t3_64x0.5k": ((64, "fixed", 512, 512),),
+    "t3_64x4k": ((64, "fixed", 4096, 4096),),
+    "t3_32x0.125k_32x4k": ((32, "fixed", 128, 128), (32, "fixed", 4096, 4096)),
+    "t3_2x32k_30x4k": ((2, "fixed", 32768, 32768), (30, "fixed", 4096, 4096)),
+    "t3_1x64k_15x4k": ((1, "fixed", 65536, 65536), (15, "fixed", 4096, 4096)),
+    "t3_1x128k_31x4k": ((1, "fixed", 131072, 131072), (31, "fixed", 4096, 4096)),
+}
+for _i, (_name, _draw) in enumerate(TABLE3.items()):
+    WORKLOADS[_name] = Workload(_name, sum(c for c, *_ in _draw), 8, 1, draw=_draw,
+                                kv_dtype="e4m3", seed=1100 + _i,
+                                description=f"Table-3 mix {_name[3:]}, FP8, Hq=8, Hkv=1")
+
+
+def draw_seqlens(w: Workload, gen: torch.Generator) -> list:
+    if w.seqlens:
+        return [int(x) for x in w.seqlens]
+    out = []
+    for count, kind, a, b in w.draw:
+        if kind == "fixed":
+            out += [int(a)] * count
+        elif kind == "uniform":
+            out += torch.randint(a, b + 1, (count,), generator=gen).tolist()
+        elif kind == "log":
+            u = torch.rand(count, generator=gen, dtype=torch.float64)
+            out += [int(math.floor(math.exp(math.log(a) + float(x) * (math.log(b) - math.log(a)))))
+                    for x in u]
+        else:
+            raise ValueError(kind)
+    return out
+
+
+@dataclass
+class Batch:
+    """One decode batch.  Tensors live on `device`; CPU copies are made on demand."""
+
+    workload: Workload
+    seqlens: torch.Tensor  # int32 [B]
+    block_table: torch.Tensor  # int32 [B, max_pages], -1 past each request's pages
+    q: torch.Tensor  # bf16 or float8_e4m3fn [B, Hq, 128]
+    k_cache: torch.Tensor  # bf16 or float8_e4m3fn [P, 64, Hkv, 128]
+    v_cache: torch.Tensor
+    q_scale: torch.Tensor | None = None  # fp32 [B, Hq] (FP8 only)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    extras: dict = field(default_factory=dict)
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def live_tokens(self) -> int:
+        return int(self.seqlens.sum().item())
+
+    def oracle_kwargs(self) -> dict:
+        w = self.workload
+        fp8 = w.kv_dtype == "e4m3"
+        return dict(num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, sm_scale=w.sm_scale,
+                    q_dtype=1 if fp8 else 0, kv_dtype=1 if fp8 else 0,
+                    q_scale=None if self.q_scale is None else self.q_scale.cpu(),
+                    k_scale=self.k_scale, v_scale=self.v_scale)
+
+
+def _normal(shape, seed, device):
+    gen = torch.Generator(device=device).manual_seed(seed)
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+
+def make_batch(w: Workload, device="cpu", seed: int | None = None, poison_tail: bool = False,
+               seqlens: list | None = None, extra_pages: int = 0) -> Batch:
+    """Draw one batch of workload `w` (optionally with explicit seqlens)."""
+    seed = w.seed if seed is None else seed
+    gen = torch.Generator().manual_seed(seed)
+    lens = draw_seqlens(w, gen) if seqlens is None else [int(x) for x in seqlens]
+    B = len(lens)
+    pages_per = [(L + PAGE - 1) // PAGE if L > 0 else 0 for L in lens]
+    total_pages = sum(pages_per) + extra_pages
+    perm = torch.randperm(max(total_pages, 1), generator=gen)[:total_pages]
+    max_pages = max(max(pages_per, default=0), 1)
+    bt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(pages_per):
+        bt[r, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    Hq, Hkv = w.num_q_heads, w.num_kv_heads
+    q32 = torch.randn((B, Hq, HEAD_DIM), generator=gen, dtype=torch.float32)
+    kv_shape = (max(total_pages, 1), PAGE, Hkv, HEAD_DIM)
+    k32 = _normal(kv_shape, seed + 1, device)
+    v32 = _normal(kv_shape, seed + 2, device)
+    fp8 = w.kv_dtype == "e4m3"
+    batch_kw = {}
+    if fp8:
+        e4m3 = torch.float8_e4m3fn
+        q_amax = q32.abs().amax(dim=-1).clamp_min(1e-12)
+        q_scale = (q_amax / 448.0).to(torch.float32)
+        q = (q32 / q_scale[..., None]).to(e4m3)
+        k_scale = float(k32.abs().max().item()) / 448.0
+        v_scale = float(v32.abs().max().item()) / 448.0
+        k = (k32 / k_scale).to(e4m3)
+        v = (v32 / v_scale).to(e4m3)
+        batch_kw = dict(q_scale=q_scale.to(device), k_scale=k_scale, v_scale=v_scale)
+    else:
+        q = q32.to(torch.bfloat16)
+        k = k32.to(torch.bfloat16)
+        v = v32.to(torch.bfloat16)
+    del k32, v32
+    if poison_tail:
+        _poison_tails(k, v, bt, lens)
+    return Batch(w, torch.tensor(lens, dtype=torch.int32).to(device), bt.to(device), q.to(device),
+                 k, v, **batch_kw)
+
+
+def _poison_tails(k, v, bt, lens):
+    """Fill the unused slots of every last page with NaN (the E4M3 NaN code for FP8)."""
+    for r, L in enumerate(lens):
+        if L <= 0 or L % PAGE == 0:
+            continue
+        page = int(bt[r, (L - 1) // PAGE])
+        for t in (k, v):
+            if t.dtype == torch.float8_e4m3fn:
+                t.view(torch.uint8)[page, L % PAGE:] = 0x7F
+            else:
+                t[page, L % PAGE:] = float("nan")
