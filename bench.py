@@ -1,0 +1,467 @@
+"""Benchmark: one decode step (assign + persistent attention + combine) of a
+synthetic mixed-length batch on GB300, timed on the device.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-static]
+
+Prints one JSON line (rank 0).  `value` is device-timed microseconds per
+step; `roofline` relates the attention kernel's algorithmic bytes per launch
+to its CUDA-event duration and the measured HBM copy peak; `e2e` is the same
+step through the host-buffer C entry point with the per-step inputs copied in
+and the output copied out inside the timed region; `cpu_baseline` is the fp64
+oracle timed on a bounded sample on the host cores; `static` is the in-house
+static split-KV schedule on the same batch.  Under torchrun every rank runs
+an independent replica (the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024  # twice the GB300 L2
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "decode-attn µs/step and achieved HBM GB/s (% of GB300 peak) on mixed-length batches"
+
+
+# ------------------------------------------------------------------ byte model
+def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc):
+    """Bytes the step must move at minimum, per kernel.
+
+    attention: every live token's K and V row of every KV head once
+      (sum_r L_r * Hkv * 128 * 2 * bpe), Q once (B * Hq * 128 * bpe, plus the
+      fp32 q-scales for FP8), and the partials it writes
+      (num_desc * G * (128 + 1) * 4);
+    combine: the partials read back plus the BF16 output (B * Hq * 128 * 2).
+    Block table, seqlens and the task map (a few KB) are not counted.
+    """
+    bpe = 1 if kv_dtype == "e4m3" else 2
+    B = len(seqlens)
+    G = Hq // Hkv
+    kv = sum(seqlens) * Hkv * 128 * 2 * bpe
+    q = B * Hq * 128 * bpe + (B * Hq * 4 if kv_dtype == "e4m3" else 0)
+    partials = num_desc * G * (128 + 1) * 4
+    out = B * Hq * 128 * 2
+    return {"kv": kv, "q": q, "partials": partials, "out": out,
+            "attn": kv + q + partials, "combine": partials + out,
+            "step": kv + q + 2 * partials + out}
+
+
+def aggregate(per_rank_us, per_rank_bytes):
+    """Replica aggregation: the step time is the slowest rank's; bytes add up."""
+    t = max(per_rank_us)
+    return t, sum(per_rank_bytes) / (t * 1e-6) / 1e9
+
+
+# ------------------------------------------------------------------ environment
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_src_hash):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_bf16_hy3_tp8.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_scaled"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "load_balanced_paged_assign_gb300", "csrc")
+    for name in ("attn_kernel.cuh", "attn_bf16.cu", "attn_fp8.cu", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples (50 ms) with host timestamps, kept while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(p[0]) for p in inside]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[4:8]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": num(inside[0][1]),
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max(num(p[2]) for p in inside)}
+
+
+# ------------------------------------------------------------------ oracle timing
+class OracleTimer:
+    """Times the oracle as it stands on bounded samples of (request, query
+    head) rows and extrapolates to the whole step by work (a row's work is its
+    live length)."""
+
+    def __init__(self, batch):
+        import numpy as np
+
+        import oracle
+        self.np, self.oracle = np, oracle
+        w = batch.workload
+        self.w = w
+        self.lens = batch.seqlens.cpu().tolist()
+        self.rows_all = np.arange(len(self.lens) * w.num_q_heads)
+        self.work = np.array([self.lens[r // w.num_q_heads] for r in self.rows_all],
+                             dtype=np.float64)
+        self.total_work = float(self.work.sum())
+        self.kw = batch.oracle_kwargs()
+        self.cpu = dict(q=batch.q.cpu(), k_cache=batch.k_cache.cpu(),
+                        v_cache=batch.v_cache.cpu(), block_table=batch.block_table.cpu(),
+                        seqlens=batch.seqlens.cpu())
+        probe = np.random.default_rng(12345).permutation(self.rows_all)[:64]
+        t = time.perf_counter()
+        self.oracle.attention(rows=probe, **self.cpu, **self.kw)
+        self.per_work = (time.perf_counter() - t) / max(float(self.work[probe].sum()), 1.0)
+
+    def run(self, budget_s, seed=0):
+        np = self.np
+        order = np.random.default_rng(seed).permutation(self.rows_all)
+        n_rows = len(order)
+        if self.per_work * self.total_work > budget_s:
+            cum = np.cumsum(self.work[order])
+            n_rows = min(int(np.searchsorted(cum, budget_s / self.per_work)) + 1, len(order))
+        rows = np.sort(order[:n_rows])
+        t = time.perf_counter()
+        self.oracle.attention(rows=rows, **self.cpu, **self.kw)
+        dt = time.perf_counter() - t
+        t = time.perf_counter()
+        self.oracle.assign_closed_form(self.lens, self.w.num_kv_heads, 152, self.w.min_tiles)
+        dt_assign = time.perf_counter() - t
+        sample_work = float(self.work[rows].sum())
+        us = (dt * self.total_work / sample_work + dt_assign) * 1e6
+        desc = (f"{len(rows)} of {len(self.rows_all)} (request, query-head) rows "
+                f"({sample_work / self.total_work:.1%} of the live-token work), fp64, "
+                f"extrapolated by work; plus the assign oracle on the full batch")
+        return us, desc
+
+
+# ------------------------------------------------------------------ main
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="hy3_tp8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-static", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--floor", type=int, default=None)
+    ap.add_argument("--ctas", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return [x]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    sample of the same workload, extrapolated by work."""
+    if rank != 0:
+        return
+    from load_balanced_paged_assign_gb300.workloads import WORKLOADS, make_batch
+    w = WORKLOADS[args.workload]
+    batch = make_batch(w, device="cpu")
+    budget = max(0.02, 150.0 / (args.steps + args.warmup))
+    timer = OracleTimer(batch)
+    per = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        us, desc = timer.run(budget, seed=i)
+        if i >= args.warmup:
+            per.append(us)
+    value = statistics.median(per)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "us/step",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": value, "unit": "us/step", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":  # host-only: no process group, rank 0 alone works
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")),
+                      int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+
+    import torch
+
+    from load_balanced_paged_assign_gb300 import _build
+    _build.build()
+    import load_balanced_paged_assign_gb300 as hd
+    from load_balanced_paged_assign_gb300.workloads import WORKLOADS, make_batch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    kv_dtype = w.kv_dtype
+    fp8 = kv_dtype == "e4m3"
+    batch = make_batch(w, device=dev)
+    B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    floor = w.min_tiles if args.floor is None else args.floor
+    ctas = args.ctas or hd.hpc_decode_num_ctas(local, hd.HPC_KV_FP8_E4M3 if fp8 else
+                                               hd.HPC_KV_BF16)
+    ws = hd.Workspace(B, Hq, Hkv, num_ctas=ctas, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(tm, part_o, part_lse, out, num_splits=0, ev=None):
+        if num_splits:
+            hd.hpc_decode_plan_static(batch.seqlens, Hkv, batch.max_pages, num_splits, tm)
+        else:
+            hd.hpc_decode_plan(batch.seqlens, Hkv, batch.max_pages, ctas, floor, tm)
+        if ev is not None:
+            ev[1].record(stream)
+        hd.hpc_decode_attn(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
+                           batch.v_scale, batch.block_table, batch.seqlens, Hq, Hkv, w.sm_scale,
+                           tm, part_o, part_lse)
+        if ev is not None:
+            ev[2].record(stream)
+        hd.hpc_decode_combine(part_o, part_lse, tm, B, Hq, Hkv, out)
+
+    def timed(n_steps, n_warm, run):
+        """Per-step device times (us) of `run(ev)`, L2 flushed before each step."""
+        for _ in range(n_warm):
+            flush.fill_(1)
+            run(None)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_steps)]
+        for ev in evs:
+            flush.fill_(1)
+            ev[0].record(stream)
+            run(ev)
+            ev[3].record(stream)
+        torch.cuda.synchronize()
+        total = [e[0].elapsed_time(e[3]) * 1e3 for e in evs]
+        attn = [e[1].elapsed_time(e[2]) * 1e3 for e in evs]
+        return total, attn
+
+    # ---- the timed region: K steps of the load-balanced schedule
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(ws.tmap, ws.part_o, ws.part_lse, ws.out)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for ev in evs:
+        flush.fill_(1)
+        ev[0].record(stream)
+        step(ws.tmap, ws.part_o, ws.part_lse, ws.out, ev=ev)
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    sampler.stop()
+    step_us = [e[0].elapsed_time(e[3]) * 1e3 for e in evs]
+    attn_us = [e[1].elapsed_time(e[2]) * 1e3 for e in evs]
+    meta = hd.hpc_decode_read_meta(ws.tmap)
+    if meta[3] != 0:
+        raise RuntimeError(f"device error flags {meta[3]}")
+    num_desc = meta[2]
+    lens = batch.seqlens.cpu().tolist()
+    nbytes = algorithmic_bytes(lens, Hq, Hkv, kv_dtype, num_desc)
+    mean_step = statistics.fmean(step_us)
+    mean_attn = statistics.fmean(attn_us)
+    all_steps = max_over_ranks(mean_step, world)
+    value, agg_gbps = aggregate(all_steps, [nbytes["step"]] * world)
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes["attn"] / (mean_attn * 1e-6) / 1e9
+    traffic = profiled_traffic(kernel_source_hash())
+    clocks = sampler.summary(t0, t1)
+
+    # ---- e2e: the same step through the host-buffer C entry point
+    e2e = None
+    if not args.no_e2e:
+        h_q = batch.q.cpu().pin_memory()
+        h_qs = batch.q_scale.cpu().pin_memory() if fp8 else None
+        h_sl = batch.seqlens.cpu().pin_memory()
+        h_bt = batch.block_table.cpu().pin_memory()
+        h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+        d_q, d_sl, d_bt = (torch.empty_like(batch.q), torch.empty_like(batch.seqlens),
+                           torch.empty_like(batch.block_table))
+        d_qs = torch.empty_like(batch.q_scale) if fp8 else None
+
+        def e2e_step(ev):
+            hd.hpc_decode_step_host(h_q, h_qs, h_sl, h_bt, h_out, d_q, d_qs, d_sl, d_bt, ws.out,
+                                    batch.k_cache, batch.v_cache, batch.k_scale, batch.v_scale,
+                                    Hq, Hkv, w.sm_scale, ctas, floor, 0, ws.tmap, ws.part_o,
+                                    ws.part_lse)
+            if ev is not None:  # attention is not separated in this path
+                ev[1].record(stream)
+                ev[2].record(stream)
+
+        n_e2e = min(args.steps, 1000)
+        tot, _ = timed(n_e2e, args.warmup, e2e_step)
+        h2d = (h_q.numel() * h_q.element_size() + h_sl.numel() * 4 + h_bt.numel() * 4 +
+               (h_qs.numel() * 4 if fp8 else 0))
+        d2h = h_out.numel() * 2
+        e2e = {"value": max(max_over_ranks(statistics.fmean(tot), world)), "unit": "us/step",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "api": "hpc_decode_step_host (pinned host buffers)"}
+
+    # ---- in-house static split-KV comparator on the same batch
+    static = None
+    if not args.no_static:
+        max_n = max(max((L + 63) // 64 for L in lens), 1)
+        s_default = min(max(1, math.ceil(ctas / (B * Hkv))), max_n)
+        sweep = sorted({s for s in (1, 2, 4, 8, 16, 32, s_default) if s <= max(max_n, 1)})
+        results = {}
+        for S in sweep:
+            sws = hd.Workspace(B, Hq, Hkv, num_splits=S, device=dev)
+            n_s = min(args.steps, 300)
+            tot, att = timed(n_s, 5, lambda ev, S=S, sws=sws: step(
+                sws.tmap, sws.part_o, sws.part_lse, sws.out, num_splits=S, ev=ev))
+            results[S] = (statistics.fmean(tot), statistics.fmean(att))
+        best = min(results, key=lambda s: results[s][0])
+        static = {"splits_default": s_default, "us_per_step_default": results[s_default][0],
+                  "best_splits": best, "us_per_step_best": results[best][0],
+                  "attn_us_best": results[best][1],
+                  "sweep_us_per_step": {str(k): round(v[0], 3) for k, v in results.items()},
+                  "dynamic_speedup_vs_best_static": results[best][0] / mean_step}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, desc = OracleTimer(batch).run(budget_s=12.0)
+        cpu_baseline = {"value": us, "unit": "us/step", "cores": os.cpu_count(),
+                        "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "batch": B,
+                   "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128, "page": 64,
+                   "live_tokens": sum(lens), "persistent_ctas": ctas, "floor": floor,
+                   "num_desc": num_desc, "budget": meta[1], "total_tiles": meta[0],
+                   "l2": "flushed before every step (256 MiB write outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "gbps": agg_gbps, "pct_of_peak": agg_gbps / (peak * world),
+        "attn_us": mean_attn, "bytes": nbytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_kernel (persistent)", "peak_kind": peak_kind,
+                     "pct_of_8tbs_nominal": achieved / 8000.0},
+        "e2e": e2e,
+        "cpu_baseline": cpu_baseline,
+        "static": static,
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * hpc_decode.h — C ABI of the load-balanced paged GQA decode-attention library
+ * (libhpcdecode.so, CUDA for sm_103a).
+ *
+ * Sources the operations are taken from (two web posts about the HPC-Ops
+ * attention backend):
+ *   [vLLM]  "騰訊混元が vLLM に HPC オプス対応" (English text of the vLLM
+ *           integration post), sections "The challenge: mixed-length decode
+ *           in every batch" and "The solution: a per-step, load-balanced
+ *           decode scheduler" (Assign / Compute and combine bullets).
+ *   [SGL]   "腾讯HPC-Ops联手SGLang开源高性能MoE内核" (SGLang integration post),
+ *           sections "Attention：变长decode的负载均衡", "围绕Live KV Work的调度"
+ *           and "从HPC-Ops Kernel到SGLang".
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers named d_* or documented as "device" are CUDA device
+ *     pointers owned by the caller.  The library never allocates or frees
+ *     memory, never synchronises a stream (except hpc_decode_read_meta) and
+ *     keeps no state between calls except a cached driver entry point.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  Launch sizes depend only on
+ *     host-known bounds, never on device data.
+ *   - The returned status covers host-side argument checks and the launch
+ *     itself (cudaGetLastError).  Problems only visible on the device (bad
+ *     seqlens, block-table entries out of range, a wait that timed out) are
+ *     OR-ed as HPC_FLAG_* bits into map->meta[3], which the caller reads after
+ *     the stream completes (hpc_decode_read_meta does that for you).
+ *   - Fixed geometry: head_dim = 128, page (= tile) size = 64 tokens,
+ *     G = Hq / Hkv query heads per KV head with 1 <= G <= 8.  Query head hq
+ *     uses KV head hq / G (contiguous groups).
+ *   - Layouts are row-major:
+ *       q         [B, Hq, 128]            bf16, or e4m3 for HPC_KV_FP8_E4M3
+ *       q_scale   [B, Hq]                 fp32 (FP8 only): q = e4m3(q8) * q_scale
+ *       k_cache,
+ *       v_cache   [num_pages, 64, Hkv, 128]  bf16 or e4m3 (k = e4m3(k8) * k_scale)
+ *       block_table [B, max_pages_per_req] int32 physical page ids; entries
+ *                 past ceil(L_r / 64) are never read
+ *       seqlens   [B] int32 live tokens per request (0 allowed)
+ *       out       [B, Hq, 128] bf16
+ *   - Base addresses of q, the caches, part_o and out must be 16-byte aligned.
+ */
+#ifndef HPC_DECODE_H
+#define HPC_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *hpc_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    HPC_OK = 0,
+    HPC_ERR_ARG = -1,         /* null pointer, negative size, misaligned pointer, bad enum */
+    HPC_ERR_UNSUPPORTED = -2, /* head_dim != 128, G > 8, Hq % Hkv != 0, too large a batch */
+    HPC_ERR_WORKSPACE = -3,   /* task-map capacity below what the plan may write */
+    HPC_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, tensor map) */
+} hpc_status;
+
+typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
+
+/* Device-side error bits, OR-ed into meta[3]. */
+#define HPC_FLAG_BAD_SEQLEN 1u   /* a seqlen < 0 or > 64 * max_pages_per_req; clamped */
+#define HPC_FLAG_DESC_OVERFLOW 2u /* the plan needed more than cap_desc descriptors */
+#define HPC_FLAG_BAD_PAGE 4u     /* a block-table entry outside [0, num_pages); page 0 read instead */
+#define HPC_FLAG_TIMEOUT 8u      /* a pipeline wait hit its time limit; output invalid */
+
+#define HPC_HEAD_DIM 128
+#define HPC_PAGE_SIZE 64
+#define HPC_MAX_GROUP 8
+#define HPC_MAX_BATCH 16384
+
+/*
+ * Task map: the device-side result of the assign step ([vLLM] Assign bullet;
+ * [SGL] 围绕Live KV Work的调度).  All arrays are caller-owned device memory.
+ *   desc        [cap_desc][4] int32 {kv_head, request, tile_begin, tile_end},
+ *               tiles local to the request, bin-major order.
+ *   bin_ptr     [num_ctas + 1] CSR offsets: CTA c drains
+ *               desc[bin_ptr[c] .. bin_ptr[c+1]); an empty range is the
+ *               terminator of an unused bin.
+ *   chunk_count [Hkv * B] descriptors per unit u = kv_head * B + request.
+ *   chunk_off   [Hkv * B] index of the unit's first descriptor; descriptor i
+ *               writes split-buffer slot i.
+ *   meta        [4] {total_tiles, budget, num_desc, error_flags}.
+ * cap_desc, cap_bins and cap_units give the sizes of desc (entries of four
+ * int32), bin_ptr and chunk_count / chunk_off, and are set by the caller.
+ * B, Hkv and num_ctas are written by the planners (the host-side struct is
+ * updated) and read by hpc_decode_attn / hpc_decode_combine, which launch
+ * num_ctas CTAs and check B and Hkv against their own arguments.
+ */
+typedef struct {
+    int32_t *desc;
+    int32_t *bin_ptr;
+    int32_t *chunk_count;
+    int32_t *chunk_off;
+    int32_t *meta;
+    int32_t cap_desc, cap_bins, cap_units;
+    int32_t B, Hkv, num_ctas;
+} hpc_task_map;
+
+/* Library version string (static storage). */
+const char *hpc_decode_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char *hpc_status_string(hpc_status status);
+
+/*
+ * Number of persistent CTAs for the attention kernel on `device`: SM count x
+ * resident CTAs per SM for that KV dtype's kernel.  Returns a negative
+ * hpc_status on failure.  ([vLLM] "persistent kernel grid")
+ */
+int32_t hpc_decode_num_ctas(int32_t device, hpc_kv_dtype kv_dtype);
+
+/*
+ * Descriptor capacity that always suffices for hpc_decode_plan:
+ * num_ctas + B * Hkv (a unit contributes one descriptor plus one per bin
+ * boundary falling inside it, and there are at most num_ctas - 1 such
+ * boundaries).  Returns -1 on negative arguments.
+ */
+int64_t hpc_decode_desc_capacity(int32_t B, int32_t Hkv, int32_t num_ctas);
+
+/* Descriptor capacity for hpc_decode_plan_static: B * Hkv * num_splits. */
+int64_t hpc_decode_static_capacity(int32_t B, int32_t Hkv, int32_t num_splits);
+
+/*
+ * Assign step ([vLLM] Assign bullet; [SGL] 围绕Live KV Work的调度): one CTA
+ * cuts every request's live KV into 64-token tiles (n_r = ceil(L_r / 64)),
+ * sums them over KV heads and requests (T = Hkv * sum n_r), sets the
+ * per-CTA budget max(ceil(T / num_ctas), min_tiles_per_cta, 1), walks tiles
+ * head-major / batch-minor and fills bins in order, spilling into the next
+ * bin when one is full.  Writes the whole task map (every bin_ptr entry,
+ * every chunk_count/chunk_off entry, desc[0 .. num_desc), meta[0..3]).
+ * The map is meant to be built once per decode step and reused by every
+ * layer's hpc_decode_attn / hpc_decode_combine.
+ *   d_seqlens          device [B] int32
+ *   B                  0 <= B <= HPC_MAX_BATCH
+ *   Hkv                >= 1
+ *   max_pages_per_req  block-table row length; a seqlen above 64 * this is
+ *                      clamped and flagged HPC_FLAG_BAD_SEQLEN
+ *   num_ctas           >= 1, the attention grid size (see hpc_decode_num_ctas)
+ *   min_tiles_per_cta  minimum-work floor (>= 0)
+ *   map                cap_desc >= hpc_decode_desc_capacity(B, Hkv, num_ctas),
+ *                      cap_bins >= num_ctas + 1 and cap_units >= B * Hkv,
+ *                      else HPC_ERR_WORKSPACE
+ */
+hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
+                           int32_t max_pages_per_req, int32_t num_ctas,
+                           int32_t min_tiles_per_cta, hpc_task_map *map, hpc_stream_t stream);
+
+/*
+ * In-house static split-KV comparator ([vLLM] "The challenge: mixed-length
+ * decode in every batch", fixed number of splits; [SGL]
+ * Attention：变长decode的负载均衡, strategy (1)).  Emits the same task-map
+ * format with one bin (= one CTA) per (kv_head, request, split):
+ * bin u * S + s of unit u = kv_head * B + request covers tiles
+ * [s * k_r, min((s + 1) * k_r, n_r)) with k_r = ceil(n_r / S); empty splits
+ * keep an empty descriptor (tile_begin == tile_end) and launch a CTA that
+ * finds no work.  The map's num_ctas becomes B * Hkv * S, which is the grid
+ * hpc_decode_attn then launches; meta[1] holds S.
+ *   num_splits  S >= 1; cap_desc >= B * Hkv * S, cap_bins >= B * Hkv * S + 1,
+ *               cap_units >= B * Hkv, else HPC_ERR_WORKSPACE.
+ */
+hpc_status hpc_decode_plan_static(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
+                                  int32_t max_pages_per_req, int32_t num_splits,
+                                  hpc_task_map *map, hpc_stream_t stream);
+
+/*
+ * Persistent attention ([vLLM] Compute and combine bullet; [SGL]
+ * 围绕Live KV Work的调度, execution paragraph): map->num_ctas CTAs; CTA c
+ * drains bin c.  For descriptor i = (h, r, tb, te) it gathers K/V pages
+ * block_table[r][tb .. te) of KV head h and computes, for the G query heads
+ * h*G .. h*G+G-1 of request r, softmax attention over tokens
+ * [64 tb, min(64 te, L_r)) with scores sm_scale * q.k, writing
+ *     part_o[i][g][:]  = sum_j p_j v_j / sum_j p_j      (fp32, normalised)
+ *     part_lse[i][g]   = log(sum_j exp(s_j))             (fp32, natural log)
+ * Empty descriptors write nothing.  FP8: scores use q_scale[r][hq] * k_scale,
+ * values v_scale; BF16 ignores the scales (pass NULL / 1).
+ *   part_o    device [map->cap_desc, G, 128] fp32
+ *   part_lse  device [map->cap_desc, G] fp32
+ *   num_pages physical pages in each cache; a live block-table entry outside
+ *             [0, num_pages) is replaced by page 0 (no out-of-bounds read) and
+ *             flags HPC_FLAG_BAD_PAGE; that request's output is then invalid.
+ */
+hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                           const hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                           hpc_stream_t stream);
+
+/*
+ * Combine ([vLLM] Compute and combine bullet: "reads the chunk count for each
+ * (head, request) pair"; [SGL] 围绕Live KV Work的调度: merge under the correct
+ * global softmax normalisation).  For every (r, hq), with unit
+ * u = (hq / G) * B + r, n = chunk_count[u], slots s = chunk_off[u] + i:
+ *     M = max_i lse_i,  w_i = exp(lse_i - M),
+ *     out[r][hq][:] = bf16_rn( sum_i w_i part_o[s_i] / sum_i w_i )
+ * A unit with no chunks (L_r = 0) gets a zero row.
+ *   d_out  device [B, Hq, 128] bf16
+ */
+hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
+                              const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t head_dim, void *d_out, hpc_stream_t stream);
+
+/*
+ * One whole decode step of one layer on device buffers: hpc_decode_plan
+ * (when num_splits == 0) or hpc_decode_plan_static (num_splits >= 1), then
+ * hpc_decode_attn and hpc_decode_combine, all on `stream`.  Arguments as in
+ * those calls.  In a real model the plan is built once per step and shared
+ * by all layers; this call rebuilds it every time.
+ */
+hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                           int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
+                           hpc_task_map *map, float *d_part_o, float *d_part_lse, void *d_out,
+                           hpc_stream_t stream);
+
+/*
+ * hpc_decode_step with the per-step inputs and the output in host memory
+ * (pinned memory makes the copies asynchronous): copies h_q, h_q_scale
+ * (FP8 only), h_seqlens and h_block_table into the caller's device staging
+ * buffers d_q, d_q_scale, d_seqlens, d_block_table, runs the step, and copies
+ * d_out back into h_out.  The KV caches stay device-resident, as they are
+ * in serving.  The host output is complete once `stream` has finished.
+ */
+hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const int32_t *h_seqlens,
+                                const int32_t *h_block_table, void *h_out, void *d_q,
+                                float *d_q_scale, int32_t *d_seqlens, int32_t *d_block_table,
+                                void *d_out, const void *d_k_cache, const void *d_v_cache,
+                                int32_t num_pages, float k_scale, float v_scale,
+                                hpc_kv_dtype kv_dtype, int32_t max_pages_per_req, int32_t B,
+                                int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                                int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
+                                hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                                hpc_stream_t stream);
+
+/*
+ * Synchronises `stream` and copies map->meta into host_meta[4]
+ * ({total_tiles, budget, num_desc, error_flags}).
+ */
+hpc_status hpc_decode_read_meta(const hpc_task_map *map, int32_t host_meta[4],
+                                hpc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HPC_DECODE_H */

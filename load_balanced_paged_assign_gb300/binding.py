@@ -1,0 +1,266 @@
+"""Python binding of the C ABI in include/hpc_decode.h (ctypes, argument marshalling only).
+
+Every function here has the name of the C entry point it forwards to and does
+nothing but turn torch tensors into pointers and sizes, call the library and
+raise on a non-zero status.  All compute happens in libhpcdecode.so; there is
+no fallback path: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+HPC_OK, HPC_ERR_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_WORKSPACE, HPC_ERR_CUDA = 0, -1, -2, -3, -4
+HPC_KV_BF16, HPC_KV_FP8_E4M3 = 0, 1
+HPC_FLAG_BAD_SEQLEN, HPC_FLAG_DESC_OVERFLOW, HPC_FLAG_BAD_PAGE, HPC_FLAG_TIMEOUT = 1, 2, 4, 8
+HEAD_DIM, PAGE_SIZE, MAX_GROUP = 128, 64, 8
+
+# Every symbol the header declares; the CPU tests check the library exports them all.
+EXPORTS = (
+    "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
+    "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
+    "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
+)
+
+
+class HpcError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+class hpc_task_map(ctypes.Structure):
+    _fields_ = [
+        ("desc", ctypes.c_void_p), ("bin_ptr", ctypes.c_void_p),
+        ("chunk_count", ctypes.c_void_p), ("chunk_off", ctypes.c_void_p),
+        ("meta", ctypes.c_void_p),
+        ("cap_desc", ctypes.c_int32), ("cap_bins", ctypes.c_int32), ("cap_units", ctypes.c_int32),
+        ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+    ]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded libhpcdecode.so; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    tm = ctypes.POINTER(hpc_task_map)
+    sig = {
+        "hpc_decode_version": (ctypes.c_char_p, []),
+        "hpc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "hpc_decode_num_ctas": (i32, [i32, ctypes.c_int]),
+        "hpc_decode_desc_capacity": (i64, [i32, i32, i32]),
+        "hpc_decode_static_capacity": (i64, [i32, i32, i32]),
+        "hpc_decode_plan": (ctypes.c_int, [vp, i32, i32, i32, i32, i32, tm, vp]),
+        "hpc_decode_plan_static": (ctypes.c_int, [vp, i32, i32, i32, i32, tm, vp]),
+        "hpc_decode_attn": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp, i32,
+                                           vp, i32, i32, i32, i32, f32, tm, vp, vp, vp]),
+        "hpc_decode_combine": (ctypes.c_int, [vp, vp, tm, i32, i32, i32, i32, vp, vp]),
+        "hpc_decode_step": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp, i32,
+                                           vp, i32, i32, i32, i32, f32, i32, i32, i32, tm, vp,
+                                           vp, vp, vp]),
+        "hpc_decode_step_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                i32, f32, f32, ctypes.c_int, i32, i32, i32, i32,
+                                                i32, f32, i32, i32, i32, tm, vp, vp, vp]),
+        "hpc_decode_read_meta": (ctypes.c_int, [tm, ctypes.POINTER(ctypes.c_int32), vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    _LIB = L
+    return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().hpc_status_string(int(status)).decode()
+    except RuntimeError:
+        return "unknown"
+
+
+def _check(fn: str, status: int):
+    if status != HPC_OK:
+        raise HpcError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def kv_dtype_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return HPC_KV_BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return HPC_KV_FP8_E4M3
+    raise TypeError(f"unsupported KV cache dtype {t.dtype}")
+
+
+class TaskMap:
+    """Caller-owned device buffers of one task map and the C struct describing them."""
+
+    def __init__(self, B: int, Hkv: int, cap_desc: int, cap_bins: int, device="cuda"):
+        dev = torch.device(device)
+        self.desc = torch.zeros((max(cap_desc, 1), 4), dtype=torch.int32, device=dev)
+        self.bin_ptr = torch.zeros(max(cap_bins, 1), dtype=torch.int32, device=dev)
+        units = max(B * Hkv, 1)
+        self.chunk_count = torch.zeros(units, dtype=torch.int32, device=dev)
+        self.chunk_off = torch.zeros(units, dtype=torch.int32, device=dev)
+        self.meta = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.c = hpc_task_map(_ptr(self.desc), _ptr(self.bin_ptr), _ptr(self.chunk_count),
+                              _ptr(self.chunk_off), _ptr(self.meta), cap_desc, cap_bins, units, 0,
+                              0, 0)
+
+    @classmethod
+    def dynamic(cls, B: int, Hkv: int, num_ctas: int, device="cuda"):
+        return cls(B, Hkv, int(lib().hpc_decode_desc_capacity(B, Hkv, num_ctas)), num_ctas + 1,
+                   device)
+
+    @classmethod
+    def static(cls, B: int, Hkv: int, num_splits: int, device="cuda"):
+        n = int(lib().hpc_decode_static_capacity(B, Hkv, num_splits))
+        return cls(B, Hkv, n, n + 1, device)
+
+    @property
+    def cap_desc(self) -> int:
+        return int(self.c.cap_desc)
+
+    @property
+    def num_ctas(self) -> int:
+        return int(self.c.num_ctas)
+
+    def to_host(self) -> dict:
+        """The map as host lists (synchronises the current stream)."""
+        meta = self.meta.tolist()
+        n = int(meta[2])
+        B, Hkv = int(self.c.B), int(self.c.Hkv)
+        return dict(total_tiles=meta[0], budget=meta[1], num_desc=n, flags=meta[3],
+                    desc=[tuple(d) for d in self.desc[:n].tolist()],
+                    bin_ptr=self.bin_ptr[:self.num_ctas + 1].tolist(),
+                    chunk_count=self.chunk_count[:B * Hkv].tolist(),
+                    chunk_off=self.chunk_off[:B * Hkv].tolist())
+
+
+def hpc_decode_version() -> str:
+    return lib().hpc_decode_version().decode()
+
+
+def hpc_decode_num_ctas(device: int = 0, kv_dtype: int = HPC_KV_BF16) -> int:
+    n = int(lib().hpc_decode_num_ctas(int(device), int(kv_dtype)))
+    if n < 0:
+        raise HpcError("hpc_decode_num_ctas", n)
+    return n
+
+
+def hpc_decode_desc_capacity(B: int, Hkv: int, num_ctas: int) -> int:
+    return int(lib().hpc_decode_desc_capacity(B, Hkv, num_ctas))
+
+
+def hpc_decode_static_capacity(B: int, Hkv: int, num_splits: int) -> int:
+    return int(lib().hpc_decode_static_capacity(B, Hkv, num_splits))
+
+
+def hpc_decode_plan(seqlens, Hkv, max_pages_per_req, num_ctas, min_tiles_per_cta, tmap: TaskMap,
+                    stream=None):
+    B = int(seqlens.numel())
+    _check("hpc_decode_plan", lib().hpc_decode_plan(
+        _ptr(seqlens), B, int(Hkv), int(max_pages_per_req), int(num_ctas),
+        int(min_tiles_per_cta), ctypes.byref(tmap.c), _stream(stream)))
+
+
+def hpc_decode_plan_static(seqlens, Hkv, max_pages_per_req, num_splits, tmap: TaskMap,
+                           stream=None):
+    B = int(seqlens.numel())
+    _check("hpc_decode_plan_static", lib().hpc_decode_plan_static(
+        _ptr(seqlens), B, int(Hkv), int(max_pages_per_req), int(num_splits),
+        ctypes.byref(tmap.c), _stream(stream)))
+
+
+def hpc_decode_attn(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens, Hq, Hkv,
+                    sm_scale, tmap: TaskMap, part_o, part_lse, stream=None):
+    _check("hpc_decode_attn", lib().hpc_decode_attn(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, float(sm_scale), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse),
+        _stream(stream)))
+
+
+def hpc_decode_combine(part_o, part_lse, tmap: TaskMap, B, Hq, Hkv, out, stream=None):
+    _check("hpc_decode_combine", lib().hpc_decode_combine(
+        _ptr(part_o), _ptr(part_lse), ctypes.byref(tmap.c), int(B), int(Hq), int(Hkv), HEAD_DIM,
+        _ptr(out), _stream(stream)))
+
+
+def hpc_decode_step(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens, Hq,
+                    Hkv, sm_scale, num_ctas, min_tiles_per_cta, num_splits, tmap: TaskMap, part_o,
+                    part_lse, out, stream=None):
+    _check("hpc_decode_step", lib().hpc_decode_step(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta), int(num_splits),
+        ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(out), _stream(stream)))
+
+
+def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d_q_scale,
+                         d_seqlens, d_block_table, d_out, k_cache, v_cache, k_scale, v_scale, Hq,
+                         Hkv, sm_scale, num_ctas, min_tiles_per_cta, num_splits, tmap: TaskMap,
+                         part_o, part_lse, stream=None):
+    _check("hpc_decode_step_host", lib().hpc_decode_step_host(
+        _ptr(h_q), _ptr(h_q_scale), _ptr(h_seqlens), _ptr(h_block_table), _ptr(h_out), _ptr(d_q),
+        _ptr(d_q_scale), _ptr(d_seqlens), _ptr(d_block_table), _ptr(d_out), _ptr(k_cache),
+        _ptr(v_cache), int(k_cache.shape[0]), float(k_scale), float(v_scale),
+        kv_dtype_of(k_cache), int(h_block_table.shape[1]), int(h_seqlens.numel()), int(Hq),
+        int(Hkv), HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta),
+        int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _stream(stream)))
+
+
+def hpc_decode_read_meta(tmap: TaskMap, stream=None) -> list:
+    host = (ctypes.c_int32 * 4)()
+    _check("hpc_decode_read_meta", lib().hpc_decode_read_meta(ctypes.byref(tmap.c), host,
+                                                              _stream(stream)))
+    return list(host)
+
+
+class Workspace:
+    """Split buffer, output and task map sized for one batch shape."""
+
+    def __init__(self, B: int, Hq: int, Hkv: int, *, num_ctas: int = 0, num_splits: int = 0,
+                 device="cuda", kv_dtype: int = HPC_KV_BF16):
+        dev = torch.device(device)
+        if num_splits:
+            self.tmap = TaskMap.static(B, Hkv, num_splits, dev)
+        else:
+            if num_ctas <= 0:
+                num_ctas = hpc_decode_num_ctas(dev.index or 0, kv_dtype)
+            self.tmap = TaskMap.dynamic(B, Hkv, num_ctas, dev)
+        self.num_ctas, self.num_splits = num_ctas, num_splits
+        G = Hq // Hkv
+        cap = max(self.tmap.cap_desc, 1)
+        self.part_o = torch.empty((cap, G, HEAD_DIM), dtype=torch.float32, device=dev)
+        self.part_lse = torch.empty((cap, G), dtype=torch.float32, device=dev)
+        self.out = torch.empty((max(B, 1), Hq, HEAD_DIM), dtype=torch.bfloat16, device=dev)

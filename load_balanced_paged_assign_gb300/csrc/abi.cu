@@ -1,0 +1,351 @@
+// Host side of the C ABI declared in include/hpc_decode.h: argument checks,
+// TMA tensor maps over the paged caches, and kernel launches.  No device
+// memory is allocated or freed here and no stream is synchronised except by
+// hpc_decode_read_meta.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+using namespace hpc;
+
+namespace {
+
+constexpr float kLog2eF = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// Per-device "dynamic shared memory attribute already raised" bits.
+std::atomic<unsigned> g_attr_done[kMaxDevices];
+
+cudaError_t prepare_kernel(const AttnConfig &cfg, int which) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned bit = 1u << which;
+    if (dev >= 0 && dev < kMaxDevices && (g_attr_done[dev].load() & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(cfg.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cfg.smem_bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) g_attr_done[dev].fetch_or(bit);
+    return e;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+hpc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA; }
+
+hpc_status check_shapes(int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                        int32_t max_pages) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages <= 0) return HPC_ERR_ARG;
+    if (head_dim != HPC_HEAD_DIM) return HPC_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0 || Hq / Hkv > HPC_MAX_GROUP) return HPC_ERR_UNSUPPORTED;
+    if (B > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
+    // every tile count and tile index must fit comfortably in int32
+    if ((int64_t)B * max_pages * Hkv >= (int64_t)1 << 30) return HPC_ERR_UNSUPPORTED;
+    return HPC_OK;
+}
+
+hpc_status check_map(const hpc_task_map *map, bool need_units) {
+    if (!map || !map->desc || !map->bin_ptr || !map->meta) return HPC_ERR_ARG;
+    if (need_units && (!map->chunk_count || !map->chunk_off)) return HPC_ERR_ARG;
+    if (map->cap_desc < 0 || map->cap_bins < 0 || map->cap_units < 0) return HPC_ERR_ARG;
+    if (!aligned16(map->desc)) return HPC_ERR_ARG;
+    return HPC_OK;
+}
+
+// Tensor map over one paged cache, [num_pages, 64, Hkv, 128].
+//  BF16: rank 5 {64 dims, 2 halves, Hkv, 64 tokens, pages}, box {64, 1, 1, 64, 1}:
+//        each load brings one 64-dim half of one head's page as 64 rows of
+//        128 B (the 128-byte swizzle span), so a row index is a token index.
+//  FP8:  rank 4 {128 dims, Hkv, 64 tokens, pages}, box {128, 1, 64, 1}.
+hpc_status make_cache_map(CUtensorMap *m, const void *base, int32_t num_pages, int32_t Hkv,
+                          bool fp8) {
+    auto encode = encoder();
+    if (!encode) return HPC_ERR_CUDA;
+    std::memset(m, 0, sizeof(*m));
+    const cuuint64_t row = (cuuint64_t)Hkv * HPC_HEAD_DIM * (fp8 ? 1 : 2);  // bytes per token
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    CUresult r;
+    if (fp8) {
+        cuuint64_t dims[4] = {HPC_HEAD_DIM, (cuuint64_t)Hkv, HPC_PAGE_SIZE, (cuuint64_t)num_pages};
+        cuuint64_t strides[3] = {HPC_HEAD_DIM, row, row * HPC_PAGE_SIZE};
+        cuuint32_t box[4] = {HPC_HEAD_DIM, 1, HPC_PAGE_SIZE, 1};
+        r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides,
+                   box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[5] = {64, 2, (cuuint64_t)Hkv, HPC_PAGE_SIZE, (cuuint64_t)num_pages};
+        cuuint64_t strides[4] = {128, 2 * 128, row, row * HPC_PAGE_SIZE};
+        cuuint32_t box[5] = {64, 1, 1, HPC_PAGE_SIZE, 1};
+        r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+                   box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS ? HPC_OK : HPC_ERR_CUDA;
+}
+
+const AttnConfig &config_for(hpc_kv_dtype dt) {
+    static const AttnConfig bf16 = attn_config_bf16();
+    static const AttnConfig fp8 = attn_config_fp8();
+    return dt == HPC_KV_FP8_E4M3 ? fp8 : bf16;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hpc_decode_version(void) { return "hpc_decode 0.1 (sm_103a)"; }
+
+const char *hpc_status_string(hpc_status s) {
+    switch (s) {
+        case HPC_OK: return "ok";
+        case HPC_ERR_ARG: return "invalid argument";
+        case HPC_ERR_UNSUPPORTED: return "unsupported shape";
+        case HPC_ERR_WORKSPACE: return "workspace too small";
+        case HPC_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int64_t hpc_decode_desc_capacity(int32_t B, int32_t Hkv, int32_t num_ctas) {
+    if (B < 0 || Hkv < 0 || num_ctas < 0) return -1;
+    return (int64_t)num_ctas + (int64_t)B * Hkv;
+}
+
+int64_t hpc_decode_static_capacity(int32_t B, int32_t Hkv, int32_t num_splits) {
+    if (B < 0 || Hkv < 0 || num_splits < 0) return -1;
+    return (int64_t)B * Hkv * num_splits;
+}
+
+int32_t hpc_decode_num_ctas(int32_t device, hpc_kv_dtype kv_dtype) {
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
+    int prev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return HPC_ERR_CUDA;
+    if (device != prev && cudaSetDevice(device) != cudaSuccess) return HPC_ERR_CUDA;
+    const AttnConfig &cfg = config_for(kv_dtype);
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = prepare_kernel(cfg, kv_dtype == HPC_KV_FP8_E4M3 ? 1 : 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kernel, kThreads,
+                                                          cfg.smem_bytes);
+    if (device != prev) cudaSetDevice(prev);
+    if (e != cudaSuccess || per_sm < 1) return HPC_ERR_CUDA;
+    return sms * per_sm;
+}
+
+hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
+                           int32_t max_pages_per_req, int32_t num_ctas,
+                           int32_t min_tiles_per_cta, hpc_task_map *map, hpc_stream_t stream) {
+    if (B < 0 || Hkv <= 0 || max_pages_per_req <= 0 || num_ctas < 1 || min_tiles_per_cta < 0)
+        return HPC_ERR_ARG;
+    if (min_tiles_per_cta >= (1 << 29)) return HPC_ERR_ARG;
+    if (B > 0 && !d_seqlens) return HPC_ERR_ARG;
+    if (B > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
+    if ((int64_t)B * max_pages_per_req * Hkv >= (int64_t)1 << 30) return HPC_ERR_UNSUPPORTED;
+    hpc_status st = check_map(map, true);
+    if (st != HPC_OK) return st;
+    if ((int64_t)num_ctas + 1 > map->cap_bins || (int64_t)B * Hkv > map->cap_units ||
+        (int64_t)map->cap_desc < hpc_decode_desc_capacity(B, Hkv, num_ctas))
+        return HPC_ERR_WORKSPACE;
+    hpc_task_map m = *map;
+    m.B = B;
+    m.Hkv = Hkv;
+    m.num_ctas = num_ctas;
+    st = cuda_status(launch_assign(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
+                                   min_tiles_per_cta, m, static_cast<cudaStream_t>(stream)));
+    if (st == HPC_OK) *map = m;
+    return st;
+}
+
+hpc_status hpc_decode_plan_static(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
+                                  int32_t max_pages_per_req, int32_t num_splits,
+                                  hpc_task_map *map, hpc_stream_t stream) {
+    if (B < 0 || Hkv <= 0 || max_pages_per_req <= 0 || num_splits < 1) return HPC_ERR_ARG;
+    if (B > 0 && !d_seqlens) return HPC_ERR_ARG;
+    if (B > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
+    if ((int64_t)B * max_pages_per_req * Hkv >= (int64_t)1 << 30) return HPC_ERR_UNSUPPORTED;
+    hpc_status st = check_map(map, true);
+    if (st != HPC_OK) return st;
+    const int64_t bins = hpc_decode_static_capacity(B, Hkv, num_splits);
+    if (bins >= ((int64_t)1 << 31) - 1) return HPC_ERR_UNSUPPORTED;
+    if (bins > map->cap_desc || bins + 1 > map->cap_bins || (int64_t)B * Hkv > map->cap_units)
+        return HPC_ERR_WORKSPACE;
+    if (bins == 0) return HPC_ERR_ARG;  // a grid needs at least one CTA
+    hpc_task_map m = *map;
+    m.B = B;
+    m.Hkv = Hkv;
+    m.num_ctas = (int32_t)bins;
+    st = cuda_status(launch_static_plan(d_seqlens, B, Hkv, max_pages_per_req, num_splits, m,
+                                        static_cast<cudaStream_t>(stream)));
+    if (st == HPC_OK) *map = m;
+    return st;
+}
+
+hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                           const hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                           hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
+    if (st != HPC_OK) return st;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (num_pages <= 0 || !d_k_cache || !d_v_cache || !d_part_o || !d_part_lse)
+        return HPC_ERR_ARG;
+    if (B > 0 && (!d_q || !d_block_table || !d_seqlens)) return HPC_ERR_ARG;
+    if (fp8 && B > 0 && !d_q_scale) return HPC_ERR_ARG;
+    if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) ||
+        !aligned16(d_part_o))
+        return HPC_ERR_ARG;
+    if (!std::isfinite(sm_scale) || (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale))))
+        return HPC_ERR_ARG;
+    st = check_map(map, false);
+    if (st != HPC_OK) return st;
+    if (map->B != B || map->Hkv != Hkv || map->num_ctas < 1 || map->num_ctas >= map->cap_bins)
+        return HPC_ERR_ARG;
+
+    CUtensorMap tk, tv;
+    st = make_cache_map(&tk, d_k_cache, num_pages, Hkv, fp8);
+    if (st == HPC_OK) st = make_cache_map(&tv, d_v_cache, num_pages, Hkv, fp8);
+    if (st != HPC_OK) return st;
+
+    AttnParams p;
+    p.bin_ptr = map->bin_ptr;
+    p.desc = reinterpret_cast<const int4 *>(map->desc);
+    p.seqlens = d_seqlens;
+    p.block_table = d_block_table;
+    p.q = d_q;
+    p.q_scale = d_q_scale;
+    p.part_o = d_part_o;
+    p.part_lse = d_part_lse;
+    p.meta = map->meta;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.max_pages = max_pages_per_req;
+    p.num_pages = num_pages;
+    p.score_scale = sm_scale * kLog2eF * (fp8 ? k_scale : 1.f);
+    p.v_scale = fp8 ? v_scale : 1.f;
+
+    const AttnConfig &cfg = config_for(kv_dtype);
+    cudaError_t e = prepare_kernel(cfg, fp8 ? 1 : 0);
+    if (e != cudaSuccess) return HPC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = fp8 ? launch_attn_fp8(tk, tv, p, map->num_ctas, s)
+            : launch_attn_bf16(tk, tv, p, map->num_ctas, s);
+    return cuda_status(e);
+}
+
+hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
+                              const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
+                              int32_t head_dim, void *d_out, hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, 1);
+    if (st != HPC_OK) return st;
+    if (!d_part_o || !d_part_lse || (B > 0 && !d_out)) return HPC_ERR_ARG;
+    if (!aligned16(d_part_o) || !aligned16(d_out)) return HPC_ERR_ARG;
+    st = check_map(map, true);
+    if (st != HPC_OK) return st;
+    if (map->B != B || map->Hkv != Hkv || (int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
+    return cuda_status(launch_combine(d_part_o, d_part_lse, *map, B, Hq, Hkv, d_out,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                           int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
+                           hpc_task_map *map, float *d_part_o, float *d_part_lse, void *d_out,
+                           hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
+    if (st != HPC_OK) return st;
+    if (num_splits < 0) return HPC_ERR_ARG;
+    st = num_splits == 0 ? hpc_decode_plan(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
+                                           min_tiles_per_cta, map, stream)
+                         : hpc_decode_plan_static(d_seqlens, B, Hkv, max_pages_per_req,
+                                                  num_splits, map, stream);
+    if (st != HPC_OK) return st;
+    st = hpc_decode_attn(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                         kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                         head_dim, sm_scale, map, d_part_o, d_part_lse, stream);
+    if (st != HPC_OK) return st;
+    return hpc_decode_combine(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, d_out, stream);
+}
+
+hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const int32_t *h_seqlens,
+                                const int32_t *h_block_table, void *h_out, void *d_q,
+                                float *d_q_scale, int32_t *d_seqlens, int32_t *d_block_table,
+                                void *d_out, const void *d_k_cache, const void *d_v_cache,
+                                int32_t num_pages, float k_scale, float v_scale,
+                                hpc_kv_dtype kv_dtype, int32_t max_pages_per_req, int32_t B,
+                                int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                                int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
+                                hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                                hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
+    if (st != HPC_OK) return st;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (B > 0 && (!h_q || !h_seqlens || !h_block_table || !h_out || !d_q || !d_seqlens ||
+                  !d_block_table || !d_out))
+        return HPC_ERR_ARG;
+    if (fp8 && B > 0 && (!h_q_scale || !d_q_scale)) return HPC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t q_bytes = (size_t)B * Hq * HPC_HEAD_DIM * (fp8 ? 1 : 2);
+    const size_t out_bytes = (size_t)B * Hq * HPC_HEAD_DIM * 2;
+    cudaError_t e = cudaSuccess;
+    if (B > 0) {
+        e = cudaMemcpyAsync(d_q, h_q, q_bytes, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess && fp8)
+            e = cudaMemcpyAsync(d_q_scale, h_q_scale, (size_t)B * Hq * sizeof(float),
+                                cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d_seqlens, h_seqlens, (size_t)B * sizeof(int32_t),
+                                cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d_block_table, h_block_table,
+                                (size_t)B * max_pages_per_req * sizeof(int32_t),
+                                cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return HPC_ERR_CUDA;
+    }
+    st = hpc_decode_step(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                         kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                         head_dim, sm_scale, num_ctas, min_tiles_per_cta, num_splits, map,
+                         d_part_o, d_part_lse, d_out, stream);
+    if (st != HPC_OK) return st;
+    if (B > 0) e = cudaMemcpyAsync(h_out, d_out, out_bytes, cudaMemcpyDeviceToHost, s);
+    return cuda_status(e);
+}
+
+hpc_status hpc_decode_read_meta(const hpc_task_map *map, int32_t host_meta[4],
+                                hpc_stream_t stream) {
+    if (!map || !map->meta || !host_meta) return HPC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_meta, map->meta, 4 * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+}  // extern "C"

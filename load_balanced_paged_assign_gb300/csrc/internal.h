@@ -1,0 +1,65 @@
+// Internal declarations shared by the kernels' translation units and the
+// host-side entry points.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "hpc_decode.h"
+
+namespace hpc {
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 64;  // tokens per tile = tokens per page
+constexpr int kMaxGroup = 8;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);  // one producer warp + consumers
+constexpr int kPlanThreads = 1024;
+
+// Stage flags written by the producer for the consumers.
+constexpr int kFirst = 1;  // first tile of a descriptor (Q is in this stage)
+constexpr int kLast = 2;   // last tile of a descriptor
+constexpr int kEnd = 4;    // terminator: the bin is drained
+
+struct AttnParams {
+    const int32_t *bin_ptr;
+    const int4 *desc;
+    const int32_t *seqlens;
+    const int32_t *block_table;
+    const void *q;
+    const float *q_scale;
+    float *part_o;
+    float *part_lse;
+    int32_t *meta;
+    int B, Hq, Hkv, G, max_pages, num_pages;
+    float score_scale;  // sm_scale * log2(e), times k_scale for FP8
+    float v_scale;      // 1 for BF16
+};
+
+// Attention kernel configuration for one KV dtype.
+struct AttnConfig {
+    const void *kernel;
+    int smem_bytes;
+    int stages;
+};
+
+AttnConfig attn_config_bf16();
+AttnConfig attn_config_fp8();
+
+cudaError_t launch_attn_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
+                             int grid, cudaStream_t s);
+cudaError_t launch_attn_fp8(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
+                            int grid, cudaStream_t s);
+
+cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages, int num_ctas,
+                          int floor, const hpc_task_map &map, cudaStream_t s);
+cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_pages,
+                               int num_splits, const hpc_task_map &map, cudaStream_t s);
+int assign_smem_bytes(int B);
+
+cudaError_t launch_combine(const float *part_o, const float *part_lse, const hpc_task_map &map,
+                           int B, int Hq, int Hkv, void *out, cudaStream_t s);
+
+}  // namespace hpc

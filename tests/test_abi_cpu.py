@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point the header declares, and rejects bad
+arguments before touching CUDA (fake, never-dereferenced device pointers)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hpc_decode.h")
+
+
+@pytest.fixture(scope="module")
+def hd():
+    from load_balanced_paged_assign_gb300 import _build
+    _build.build()
+    import load_balanced_paged_assign_gb300 as pkg
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hpc_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree(hd):
+    assert declared_functions() == sorted(hd.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(hd):
+    L = hd.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert "sm_103a" in hd.hpc_decode_version()
+
+
+def test_capacities(hd):
+    assert hd.hpc_decode_desc_capacity(4, 1, 132) == 136
+    assert hd.hpc_decode_desc_capacity(64, 8, 152) == 152 + 512
+    assert hd.hpc_decode_static_capacity(64, 8, 4) == 2048
+    assert hd.hpc_decode_desc_capacity(-1, 1, 1) == -1
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced on the host
+
+
+def fake_map(hd, cap_desc=200, cap_bins=200, cap_units=64):
+    m = hd.binding.hpc_task_map(FAKE, FAKE, FAKE, FAKE, FAKE, cap_desc, cap_bins, cap_units, 0, 0,
+                                0)
+    return m
+
+
+def call_plan(hd, B=4, Hkv=1, max_pages=32, ctas=132, floor=2, m=None, seqlens=FAKE):
+    m = m if m is not None else fake_map(hd)
+    return hd.lib().hpc_decode_plan(seqlens, B, Hkv, max_pages, ctas, floor, ctypes.byref(m),
+                                    None)
+
+
+def test_plan_argument_checks(hd):
+    assert call_plan(hd, B=-1) == hd.binding.HPC_ERR_ARG
+    assert call_plan(hd, Hkv=0) == hd.binding.HPC_ERR_ARG
+    assert call_plan(hd, ctas=0) == hd.binding.HPC_ERR_ARG
+    assert call_plan(hd, floor=-1) == hd.binding.HPC_ERR_ARG
+    assert call_plan(hd, seqlens=None) == hd.binding.HPC_ERR_ARG
+    assert call_plan(hd, B=20000) == hd.binding.HPC_ERR_UNSUPPORTED
+    # capacities: desc below num_ctas + B*Hkv, bin_ptr below num_ctas + 1, units below B*Hkv
+    assert call_plan(hd, m=fake_map(hd, cap_desc=135)) == hd.binding.HPC_ERR_WORKSPACE
+    assert call_plan(hd, m=fake_map(hd, cap_bins=132)) == hd.binding.HPC_ERR_WORKSPACE
+    assert call_plan(hd, B=8, Hkv=8, m=fake_map(hd, cap_desc=500, cap_units=63)) == \
+        hd.binding.HPC_ERR_WORKSPACE
+    bad = fake_map(hd)
+    bad.desc = FAKE + 4  # misaligned descriptor array
+    assert call_plan(hd, m=bad) == hd.binding.HPC_ERR_ARG
+    bad = fake_map(hd)
+    bad.meta = None
+    assert call_plan(hd, m=bad) == hd.binding.HPC_ERR_ARG
+
+
+def test_static_plan_argument_checks(hd):
+    L = hd.lib()
+    m = fake_map(hd, cap_desc=16, cap_bins=17, cap_units=4)
+    assert L.hpc_decode_plan_static(FAKE, 4, 1, 8, 0, ctypes.byref(m), None) == \
+        hd.binding.HPC_ERR_ARG
+    assert L.hpc_decode_plan_static(FAKE, 4, 1, 8, 5, ctypes.byref(m), None) == \
+        hd.binding.HPC_ERR_WORKSPACE
+    m = fake_map(hd, cap_desc=16, cap_bins=16, cap_units=4)
+    assert L.hpc_decode_plan_static(FAKE, 4, 1, 8, 4, ctypes.byref(m), None) == \
+        hd.binding.HPC_ERR_WORKSPACE
+
+
+def call_attn(hd, m, q=FAKE, q_scale=None, k=FAKE, v=FAKE, num_pages=10, dtype=0, bt=FAKE,
+              max_pages=4, seqlens=FAKE, B=4, Hq=8, Hkv=1, D=128, sm=0.088, po=FAKE, pl=FAKE):
+    return hd.lib().hpc_decode_attn(q, q_scale, k, v, num_pages, 1.0, 1.0, dtype, bt, max_pages,
+                                    seqlens, B, Hq, Hkv, D, sm, ctypes.byref(m), po, pl, None)
+
+
+def test_attn_argument_checks(hd):
+    m = fake_map(hd)
+    m.B, m.Hkv, m.num_ctas = 4, 1, 132
+    E = hd.binding
+    assert call_attn(hd, m, D=64) == E.HPC_ERR_UNSUPPORTED
+    assert call_attn(hd, m, Hq=12, Hkv=1) == E.HPC_ERR_UNSUPPORTED  # G = 12 > 8
+    assert call_attn(hd, m, Hq=10, Hkv=4) == E.HPC_ERR_UNSUPPORTED  # Hq % Hkv != 0
+    assert call_attn(hd, m, q=FAKE + 8) == E.HPC_ERR_ARG  # misaligned Q
+    assert call_attn(hd, m, k=FAKE + 2) == E.HPC_ERR_ARG
+    assert call_attn(hd, m, num_pages=0) == E.HPC_ERR_ARG
+    assert call_attn(hd, m, dtype=7) == E.HPC_ERR_ARG
+    assert call_attn(hd, m, dtype=1) == E.HPC_ERR_ARG  # FP8 without q_scale
+    assert call_attn(hd, m, sm=float("nan")) == E.HPC_ERR_ARG
+    assert call_attn(hd, m, B=5) == E.HPC_ERR_ARG  # map planned for another batch
+    m.num_ctas = 0
+    assert call_attn(hd, m) == E.HPC_ERR_ARG  # map never planned
+
+
+def test_combine_argument_checks(hd):
+    m = fake_map(hd)
+    m.B, m.Hkv, m.num_ctas = 4, 1, 132
+    L = hd.lib()
+    E = hd.binding
+    assert L.hpc_decode_combine(FAKE, FAKE, ctypes.byref(m), 4, 8, 1, 256, FAKE, None) == \
+        E.HPC_ERR_UNSUPPORTED
+    assert L.hpc_decode_combine(FAKE, FAKE, ctypes.byref(m), 4, 8, 1, 128, FAKE + 4, None) == \
+        E.HPC_ERR_ARG
+    assert L.hpc_decode_combine(None, FAKE, ctypes.byref(m), 4, 8, 1, 128, FAKE, None) == \
+        E.HPC_ERR_ARG
+    assert L.hpc_decode_combine(FAKE, FAKE, ctypes.byref(m), 3, 8, 1, 128, FAKE, None) == \
+        E.HPC_ERR_ARG
+
+
+def test_status_strings(hd):
+    assert hd.binding.status_string(0) == "ok"
+    assert hd.binding.status_string(-3) == "workspace too small"

@@ -1,0 +1,214 @@
+"""GPU decode attention (plan + persistent attention + combine, through the
+C ABI) against the fp64 oracle.
+
+Small cases are compared element by element; the full-size workloads run in
+the launch configuration the benchmark times (persistent CTAs = what the
+device holds, floor 2) and are compared on every row (hy3_tp8) or on sampled
+rows the oracle computes one by one (the rest)."""
+
+import numpy as np
+import pytest
+import torch
+
+import load_balanced_paged_assign_gb300 as hd
+from _gpu import TOL, assert_close, assert_map_matches, device_ctas, oracle_out, run_step
+from load_balanced_paged_assign_gb300.workloads import WORKLOADS, Workload, make_batch
+
+pytestmark = pytest.mark.gpu
+
+BOUNDARY_LENS = [1, 63, 64, 65, 127, 128, 129, 300, 1000, 4097]
+
+
+def small(B, hq, hkv, kv_dtype="bf16", floor=2, ctas=0):
+    return Workload("small", B, hq, hkv, seqlens=tuple([1] * B), kv_dtype=kv_dtype, seed=77,
+                    min_tiles=floor, num_ctas=ctas)
+
+
+def test_tiny_workload_full_parity():
+    w = WORKLOADS["tiny"]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), w.num_kv_heads, w.num_ctas, w.min_tiles)
+    assert_close(out, oracle_out(batch), "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("hq,hkv", [(8, 1), (8, 2), (16, 2), (4, 1), (1, 1), (64, 8), (6, 3)])
+@pytest.mark.parametrize("ctas", [1, 7, 0])
+def test_small_shapes(kv_dtype, hq, hkv, ctas):
+    w = small(len(BOUNDARY_LENS), hq, hkv, kv_dtype, ctas=ctas)
+    batch = make_batch(w, device="cuda", seqlens=BOUNDARY_LENS, poison_tail=True,
+                       seed=100 + hq + hkv)
+    out, _ = run_step(batch)
+    assert_close(out, oracle_out(batch), kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("floor", [0, 1, 4, 1000])
+def test_floor_values(kv_dtype, floor):
+    lens = [3000, 17, 64, 9000, 1]
+    w = small(len(lens), 8, 1, kv_dtype, floor=floor)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=5)
+    out, ws = run_step(batch, num_ctas=40)
+    assert_map_matches(ws, lens, 1, 40, floor)
+    assert_close(out, oracle_out(batch), kv_dtype)
+
+
+def test_length_one_returns_v_row_bitwise():
+    w = small(3, 8, 1)
+    batch = make_batch(w, device="cuda", seqlens=[1, 1, 1], seed=9)
+    out, _ = run_step(batch)
+    for r in range(3):
+        page = int(batch.block_table[r, 0])
+        v0 = batch.v_cache[page, 0, 0]
+        for hq in range(8):
+            assert torch.equal(out[r, hq], v0)
+
+
+def test_constant_v_returns_that_row():
+    w = small(4, 8, 2)
+    batch = make_batch(w, device="cuda", seqlens=[77, 300, 4096, 1], seed=3)
+    row = torch.linspace(-3, 3, 128, device="cuda").to(torch.bfloat16)
+    batch.v_cache[:] = row
+    out, _ = run_step(batch, num_ctas=16)
+    err = (out.float() - row.float()).abs().max().item()
+    assert err <= 2 ** -7 * 3  # one bf16 rounding of |row| <= 3
+
+
+def test_zero_length_requests_give_zero_rows():
+    lens = [0, 100, 0, 5000]
+    w = small(4, 8, 1)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=4)
+    out, _ = run_step(batch, num_ctas=9)
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+    assert_close(out, oracle_out(batch), "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_deterministic_and_page_permutation_invariant(kv_dtype):
+    lens = [5000, 70, 1300, 64]
+    w = small(4, 8, 2, kv_dtype)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=6)
+    a, _ = run_step(batch, num_ctas=20)
+    b, _ = run_step(batch, num_ctas=20)
+    assert torch.equal(a, b)
+    P = batch.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(2)).cuda()
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P, device="cuda")
+    batch.k_cache = batch.k_cache[perm].contiguous()
+    batch.v_cache = batch.v_cache[perm].contiguous()
+    bt = batch.block_table.clone()
+    live = bt >= 0
+    bt[live] = inv[bt[live].long()].to(torch.int32)
+    batch.block_table = bt
+    c, _ = run_step(batch, num_ctas=20)
+    assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_static_schedule_parity(kv_dtype, S):
+    w = small(len(BOUNDARY_LENS), 8, 2, kv_dtype)
+    batch = make_batch(w, device="cuda", seqlens=BOUNDARY_LENS, poison_tail=True, seed=11)
+    out, ws = run_step(batch, num_splits=S)
+    assert ws.tmap.to_host()["flags"] == 0
+    assert_close(out, oracle_out(batch), kv_dtype)
+
+
+def test_bad_page_is_flagged_not_read_out_of_bounds():
+    w = small(2, 8, 1)
+    batch = make_batch(w, device="cuda", seqlens=[200, 100], seed=8)
+    batch.block_table[0, 1] = batch.num_pages + 5
+    out, ws = run_step(batch, num_ctas=4)
+    flags = hd.hpc_decode_read_meta(ws.tmap)[3]
+    assert flags & hd.binding.HPC_FLAG_BAD_PAGE
+    ref = oracle_out(make_batch(w, device="cuda", seqlens=[200, 100], seed=8))
+    assert_close(out[1:], ref[1:], "bf16")  # the other request is unaffected
+
+
+def test_host_buffer_step_matches_device_step():
+    w = WORKLOADS["tiny"]
+    batch = make_batch(w, device="cuda")
+    dev_out, _ = run_step(batch)
+    B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    h_q = batch.q.cpu().pin_memory()
+    h_sl = batch.seqlens.cpu().pin_memory()
+    h_bt = batch.block_table.cpu().pin_memory()
+    h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+    d_q, d_sl, d_bt = torch.empty_like(batch.q), torch.empty_like(batch.seqlens), \
+        torch.empty_like(batch.block_table)
+    ws = hd.Workspace(B, Hq, Hkv, num_ctas=w.num_ctas)
+    hd.hpc_decode_step_host(h_q, None, h_sl, h_bt, h_out, d_q, None, d_sl, d_bt, ws.out,
+                            batch.k_cache, batch.v_cache, 1.0, 1.0, Hq, Hkv, w.sm_scale,
+                            w.num_ctas, w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out, dev_out.cpu())
+
+
+def sample_rows(batch, n_random, seed, must_rows=()):
+    w = batch.workload
+    total = len(batch.seqlens) * w.num_q_heads
+    rng = np.random.default_rng(seed)
+    rows = set(int(x) for x in rng.choice(total, size=min(n_random, total), replace=False))
+    rows.update(must_rows)
+    return sorted(rows)
+
+
+@pytest.mark.slow
+def test_hy3_tp8_full_parity():
+    w = WORKLOADS["hy3_tp8"]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), w.num_kv_heads, device_ctas("bf16"),
+                       w.min_tiles)
+    assert_close(out, oracle_out(batch), "bf16")
+
+
+@pytest.mark.slow
+def test_skewed_sampled_parity():
+    w = WORKLOADS["skewed"]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), w.num_kv_heads, device_ctas("bf16"),
+                       w.min_tiles)
+    lens = batch.seqlens.tolist()
+    long_reqs = [r for r, L in enumerate(lens) if L > 60000]
+    # every query head of one long request, one head of each other long request
+    must = [long_reqs[0] * 64 + hq for hq in range(64)] + [r * 64 + 5 for r in long_reqs[1:]]
+    rows = sample_rows(batch, 192, 1, must)
+    assert_close(out, oracle_out(batch, rows=rows), "bf16", rows=rows)
+
+
+@pytest.mark.slow
+def test_uniform_sampled_parity():
+    w = WORKLOADS["uniform"]
+    batch = make_batch(w, device="cuda")
+    out, _ = run_step(batch)
+    rows = sample_rows(batch, 160, 2)
+    assert_close(out, oracle_out(batch, rows=rows), "bf16", rows=rows)
+
+
+@pytest.mark.slow
+def test_fp8_sampled_parity():
+    w = WORKLOADS["fp8"]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), w.num_kv_heads, device_ctas("e4m3"),
+                       w.min_tiles)
+    lens = batch.seqlens.tolist()
+    longest = int(np.argmax(lens))
+    rows = sample_rows(batch, 128, 3, [longest * 8 + h for h in range(8)])
+    assert_close(out, oracle_out(batch, rows=rows), "e4m3", rows=rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["t3_32x0.125k_32x4k", "t3_1x128k_31x4k"])
+def test_table3_mixes_parity(name):
+    w = WORKLOADS[name]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, _ = run_step(batch)
+    rows = sample_rows(batch, 64, 4, list(range(8)))
+    assert_close(out, oracle_out(batch, rows=rows), "e4m3", rows=rows)
+    static, _ = run_step(batch, num_splits=4)
+    assert_close(static, oracle_out(batch, rows=rows), "e4m3", rows=rows)
