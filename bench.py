@@ -245,7 +245,8 @@ def max_over_ranks(x, world):
         return [x]
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     out = [torch.zeros_like(t) for _ in range(world)]
     dist.all_gather(out, t)
     return [float(o.item()) for o in out]
