@@ -241,6 +241,44 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
                                 hpc_stream_t stream);
 
 /*
+ * Size of the scratch array compiled into the library for
+ * hpc_decode_step_noalloc.
+ */
+#define HPC_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * hpc_decode_step for callers that cannot allocate device memory.  The
+ * posts describe nothing like it; it exists for callers that may not call
+ * cudaMalloc when they run attention (code under an allocator they do not
+ * own, plug-ins whose host forbids device allocation after start-up, tools
+ * that must leave the memory state untouched).  They pass only the inputs
+ * and the output; the task map and the split buffer live in one
+ * HPC_NOALLOC_SCRATCH_BYTES array inside the library, which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing and frees nothing.
+ *   Arguments as in hpc_decode_step (load-balanced plan only), plus
+ *   d_out       device [B, Hq, 128] bf16, written
+ *   d_meta_out  device int32[4] or NULL: receives the step's
+ *               {total_tiles, budget, num_desc, error_flags}
+ * Limits: the scratch must hold (num_ctas + B*Hkv) descriptors with their
+ * partials, about 4.2 KB each at G = 8 (roughly 1,900 descriptors);
+ * larger problems get HPC_ERR_WORKSPACE before anything is launched.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array and leave their contents in it: calls that
+ * overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.
+ */
+hpc_status hpc_decode_step_noalloc(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                                   const void *d_v_cache, int32_t num_pages, float k_scale,
+                                   float v_scale, hpc_kv_dtype kv_dtype,
+                                   const int32_t *d_block_table, int32_t max_pages_per_req,
+                                   const int32_t *d_seqlens, int32_t B, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim, float sm_scale, int32_t num_ctas,
+                                   int32_t min_tiles_per_cta, void *d_out, int32_t *d_meta_out,
+                                   hpc_stream_t stream);
+
+/*
  * Synchronises `stream` and copies map->meta into host_meta[4]
  * ({total_tiles, budget, num_desc, error_flags}).
  */

@@ -25,6 +25,7 @@ EXPORTS = (
     "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
     "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
     "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
+    "hpc_decode_step_noalloc",
 )
 
 
@@ -81,6 +82,9 @@ def lib():
                                                 i32, f32, f32, ctypes.c_int, i32, i32, i32, i32,
                                                 i32, f32, i32, i32, i32, tm, vp, vp, vp]),
         "hpc_decode_read_meta": (ctypes.c_int, [tm, ctypes.POINTER(ctypes.c_int32), vp]),
+        "hpc_decode_step_noalloc": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
+                                                   vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
+                                                   vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -244,6 +248,18 @@ def hpc_decode_read_meta(tmap: TaskMap, stream=None) -> list:
     _check("hpc_decode_read_meta", lib().hpc_decode_read_meta(ctypes.byref(tmap.c), host,
                                                               _stream(stream)))
     return list(host)
+
+
+def hpc_decode_step_noalloc(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens,
+                            Hq, Hkv, sm_scale, num_ctas, min_tiles_per_cta, out, meta_out=None,
+                            stream=None):
+    """Whole step with the library's built-in scratch; see the C header."""
+    _check("hpc_decode_step_noalloc", lib().hpc_decode_step_noalloc(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta), _ptr(out),
+        _ptr(meta_out), _stream(stream)))
 
 
 class Workspace:
