@@ -37,26 +37,31 @@ METRIC = "decode-attn µs/step and achieved HBM GB/s (% of GB300 peak) on mixed-
 
 
 # ------------------------------------------------------------------ byte model
-def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc):
-    """Bytes the step must move at minimum, per kernel.
+def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc, split_desc):
+    """Bytes each kernel must move at minimum.
 
-    attention: every live token's K and V row of every KV head once
-      (sum_r L_r * Hkv * 128 * 2 * bpe), Q once (B * Hq * 128 * bpe, plus the
-      fp32 q-scales for FP8), and the partials it writes
-      (num_desc * G * (128 + 1) * 4);
-    combine: the partials read back plus the BF16 output (B * Hq * 128 * 2).
-    Block table, seqlens and the task map (a few KB) are not counted.
+    KV: every live token's K and V row of every KV head once,
+      sum_r L_r * Hkv * 128 * 2 * bpe;  Q: B * Hq * 128 * bpe (+ fp32 q-scales
+      for FP8);  out: B * Hq * 128 * 2;  a partial: G * (128 + 1) * 4.
+    attn (separate combine): KV + Q + one partial written per descriptor.
+    combine: those partials read + out.
+    attn_fused (the launch the roofline uses): KV + Q + out + the partials of
+      split units written and read back (a unit with one chunk writes its
+      output directly).
+    step: the timed step, assign + fused attention (the task map is a few KB).
+    Block table and seqlens (a few KB) are not counted.
     """
     bpe = 1 if kv_dtype == "e4m3" else 2
     B = len(seqlens)
     G = Hq // Hkv
     kv = sum(seqlens) * Hkv * 128 * 2 * bpe
     q = B * Hq * 128 * bpe + (B * Hq * 4 if kv_dtype == "e4m3" else 0)
-    partials = num_desc * G * (128 + 1) * 4
+    part = G * (128 + 1) * 4
     out = B * Hq * 128 * 2
-    return {"kv": kv, "q": q, "partials": partials, "out": out,
-            "attn": kv + q + partials, "combine": partials + out,
-            "step": kv + q + 2 * partials + out}
+    fused = kv + q + out + 2 * split_desc * part
+    return {"kv": kv, "q": q, "partials": num_desc * part, "out": out,
+            "attn": kv + q + num_desc * part, "combine": num_desc * part + out,
+            "attn_fused": fused, "step": fused}
 
 
 def aggregate(per_rank_us, per_rank_bytes):
@@ -219,6 +224,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--floor", type=int, default=None)
     ap.add_argument("--ctas", type=int, default=0)
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step from a CUDA graph instead of launching its kernels")
+    ap.add_argument("--bins-per-cta", type=int, default=1,
+                    help="bins planned per persistent CTA (1 = one bin per CTA)")
     return ap.parse_args()
 
 
@@ -306,79 +315,128 @@ def main():
     batch = make_batch(w, device=dev)
     B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
     floor = w.min_tiles if args.floor is None else args.floor
-    ctas = args.ctas or hd.hpc_decode_num_ctas(local, hd.HPC_KV_FP8_E4M3 if fp8 else
-                                               hd.HPC_KV_BF16)
+    resident = hd.hpc_decode_num_ctas(local, hd.HPC_KV_FP8_E4M3 if fp8 else hd.HPC_KV_BF16)
+    ctas = args.ctas or resident * args.bins_per_cta  # bins of the plan
     ws = hd.Workspace(B, Hq, Hkv, num_ctas=ctas, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    capture_stream = torch.cuda.Stream(device=dev)
 
-    def step(tm, part_o, part_lse, out, num_splits=0, ev=None):
+    def plan(tm, num_splits=0):
         if num_splits:
             hd.hpc_decode_plan_static(batch.seqlens, Hkv, batch.max_pages, num_splits, tm)
         else:
             hd.hpc_decode_plan(batch.seqlens, Hkv, batch.max_pages, ctas, floor, tm)
-        if ev is not None:
-            ev[1].record(stream)
-        hd.hpc_decode_attn(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
-                           batch.v_scale, batch.block_table, batch.seqlens, Hq, Hkv, w.sm_scale,
-                           tm, part_o, part_lse)
-        if ev is not None:
-            ev[2].record(stream)
-        hd.hpc_decode_combine(part_o, part_lse, tm, B, Hq, Hkv, out)
+
+    def attention(w_s, fused=True):
+        if fused:
+            hd.hpc_decode_attn_combine(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
+                                       batch.k_scale, batch.v_scale, batch.block_table,
+                                       batch.seqlens, Hq, Hkv, w.sm_scale, w_s.tmap, w_s.part_o,
+                                       w_s.part_lse, w_s.unit_done, w_s.out)
+        else:
+            hd.hpc_decode_attn(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
+                               batch.k_scale, batch.v_scale, batch.block_table, batch.seqlens,
+                               Hq, Hkv, w.sm_scale, w_s.tmap, w_s.part_o, w_s.part_lse)
+            hd.hpc_decode_combine(w_s.part_o, w_s.part_lse, w_s.tmap, B, Hq, Hkv, w_s.out)
+
+    def step(w_s, num_splits=0, fused=True):
+        plan(w_s.tmap, num_splits)
+        attention(w_s, fused)
+
+    def graphed(fn):
+        """fn captured once into a CUDA graph (the programmatic launch edges between
+        the kernels are kept); returns a replay function."""
+        fn()  # first call outside capture: one-time attribute and occupancy set-up
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=capture_stream):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
 
     def timed(n_steps, n_warm, run):
-        """Per-step device times (us) of `run(ev)`, L2 flushed before each step."""
+        """Per-step device times (us) of run(), L2 flushed before each step; no
+        event sits between the kernels of a step, so programmatic launches overlap."""
         for _ in range(n_warm):
             flush.fill_(1)
-            run(None)
+            run()
         torch.cuda.synchronize()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_steps)]
-        for ev in evs:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_steps)]
+        for e0, e1 in evs:
             flush.fill_(1)
-            ev[0].record(stream)
-            run(ev)
-            ev[3].record(stream)
+            e0.record(stream)
+            run()
+            e1.record(stream)
         torch.cuda.synchronize()
-        total = [e[0].elapsed_time(e[3]) * 1e3 for e in evs]
-        attn = [e[1].elapsed_time(e[2]) * 1e3 for e in evs]
-        return total, attn
+        return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
 
-    # ---- the timed region: K steps of the load-balanced schedule
+    # ---- the timed region: K decode steps (assign + attention with fused combine),
+    # launched directly (or replayed from a CUDA graph with --graph)
+    run_step = graphed(lambda: step(ws)) if args.graph else (lambda: step(ws))
     sampler = ClockSampler(local)
     for _ in range(args.warmup):
         flush.fill_(1)
-        step(ws.tmap, ws.part_o, ws.part_lse, ws.out)
+        run_step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    for ev in evs:
+    for e0, e1 in evs:
         flush.fill_(1)
-        ev[0].record(stream)
-        step(ws.tmap, ws.part_o, ws.part_lse, ws.out, ev=ev)
-        ev[3].record(stream)
+        e0.record(stream)
+        run_step()
+        e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
     sampler.stop()
-    step_us = [e[0].elapsed_time(e[3]) * 1e3 for e in evs]
-    attn_us = [e[1].elapsed_time(e[2]) * 1e3 for e in evs]
+    step_us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
     meta = hd.hpc_decode_read_meta(ws.tmap)
     if meta[3] != 0:
         raise RuntimeError(f"device error flags {meta[3]}")
     num_desc = meta[2]
     lens = batch.seqlens.cpu().tolist()
-    nbytes = algorithmic_bytes(lens, Hq, Hkv, kv_dtype, num_desc)
+    counts = ws.tmap.chunk_count[:B * Hkv].tolist()
+    split_desc = sum(c for c in counts if c > 1)
+    nbytes = algorithmic_bytes(lens, Hq, Hkv, kv_dtype, num_desc, split_desc)
     mean_step = statistics.fmean(step_us)
-    mean_attn = statistics.fmean(attn_us)
     all_steps = max_over_ranks(mean_step, world)
     value, agg_gbps = aggregate(all_steps, [nbytes["step"]] * world)
-
-    peak, peak_kind = measured_peaks()
-    achieved = nbytes["attn"] / (mean_attn * 1e-6) / 1e9
-    traffic = profiled_traffic(kernel_source_hash())
     clocks = sampler.summary(t0, t1)
+
+    # ---- the dominant kernel alone, as every layer runs it on the step's map:
+    # flush, rebuild the map (untimed, so it sits in L2 as in a model where all
+    # layers share it), then time the attention launch by itself
+    def attn_alone(n_steps, n_warm, w_s, num_splits=0):
+        for _ in range(n_warm):
+            flush.fill_(1)
+            step(w_s, num_splits)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_steps)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            plan(w_s.tmap, num_splits)
+            e0.record(stream)
+            attention(w_s)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+
+    attn_us_list = attn_alone(args.steps, args.warmup, ws)
+    mean_attn = statistics.fmean(attn_us_list)
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes["attn_fused"] / (mean_attn * 1e-6) / 1e9
+    traffic = profiled_traffic(kernel_source_hash())
+
+    # ---- the same step with the combine as its own kernel
+    n_unf = min(args.steps, 1000)
+    unf = graphed(lambda: step(ws, fused=False)) if args.graph else (lambda: step(ws, fused=False))
+    unfused_us = statistics.fmean(timed(n_unf, args.warmup, unf))
 
     # ---- e2e: the same step through the host-buffer C entry point
     e2e = None
@@ -392,17 +450,14 @@ def main():
                            torch.empty_like(batch.block_table))
         d_qs = torch.empty_like(batch.q_scale) if fp8 else None
 
-        def e2e_step(ev):
+        def e2e_step():
             hd.hpc_decode_step_host(h_q, h_qs, h_sl, h_bt, h_out, d_q, d_qs, d_sl, d_bt, ws.out,
                                     batch.k_cache, batch.v_cache, batch.k_scale, batch.v_scale,
                                     Hq, Hkv, w.sm_scale, ctas, floor, 0, ws.tmap, ws.part_o,
-                                    ws.part_lse)
-            if ev is not None:  # attention is not separated in this path
-                ev[1].record(stream)
-                ev[2].record(stream)
+                                    ws.part_lse, ws.unit_done)
 
         n_e2e = min(args.steps, 1000)
-        tot, _ = timed(n_e2e, args.warmup, e2e_step)
+        tot = timed(n_e2e, args.warmup, e2e_step)
         h2d = (h_q.numel() * h_q.element_size() + h_sl.numel() * 4 + h_bt.numel() * 4 +
                (h_qs.numel() * 4 if fp8 else 0))
         d2h = h_out.numel() * 2
@@ -420,15 +475,16 @@ def main():
         for S in sweep:
             sws = hd.Workspace(B, Hq, Hkv, num_splits=S, device=dev)
             n_s = min(args.steps, 300)
-            tot, att = timed(n_s, 5, lambda ev, S=S, sws=sws: step(
-                sws.tmap, sws.part_o, sws.part_lse, sws.out, num_splits=S, ev=ev))
+            tot = timed(n_s, 5, lambda sws=sws, S=S: step(sws, num_splits=S))
+            att = attn_alone(n_s, 5, sws, S)
             results[S] = (statistics.fmean(tot), statistics.fmean(att))
         best = min(results, key=lambda s: results[s][0])
         static = {"splits_default": s_default, "us_per_step_default": results[s_default][0],
                   "best_splits": best, "us_per_step_best": results[best][0],
                   "attn_us_best": results[best][1],
                   "sweep_us_per_step": {str(k): round(v[0], 3) for k, v in results.items()},
-                  "dynamic_speedup_vs_best_static": results[best][0] / mean_step}
+                  "dynamic_speedup_vs_best_static": results[best][0] / mean_step,
+                  "dynamic_attn_speedup_vs_best_static": results[best][1] / mean_attn}
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -445,21 +501,24 @@ def main():
         "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "description": w.description, "batch": B,
                    "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128, "page": 64,
-                   "live_tokens": sum(lens), "persistent_ctas": ctas, "floor": floor,
+                   "live_tokens": sum(lens), "persistent_ctas": min(ctas, resident),
+                   "bins": ctas, "floor": floor,
                    "num_desc": num_desc, "budget": meta[1], "total_tiles": meta[0],
                    "l2": "flushed before every step (256 MiB write outside the events)",
                    "parallelism": f"replicas x{world}"},
         "gbps": agg_gbps, "pct_of_peak": agg_gbps / (peak * world),
-        "attn_us": mean_attn, "bytes": nbytes,
+        "attn_us": mean_attn, "unfused_us_per_step": unfused_us,
+        "launch": "cuda graph replay per step" if args.graph else "direct launches", "bytes": nbytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "attn_kernel (persistent)", "peak_kind": peak_kind,
+                     "kernel": "attn_kernel, fused combine (per-layer launch)",
+                     "peak_kind": peak_kind,
                      "pct_of_8tbs_nominal": achieved / 8000.0},
         "e2e": e2e,
         "cpu_baseline": cpu_baseline,
         "static": static,
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
     }
     print(json.dumps(line), flush=True)
 

@@ -83,12 +83,23 @@ typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
  *   chunk_count [Hkv * B] descriptors per unit u = kv_head * B + request.
  *   chunk_off   [Hkv * B] index of the unit's first descriptor; descriptor i
  *               writes split-buffer slot i.
- *   meta        [4] {total_tiles, budget, num_desc, error_flags}.
+ *   meta        [8] {total_tiles, budget, num_desc, error_flags, bin counter,
+ *               reserved x3}; the bin counter is zeroed by the planners and
+ *               left zero by every attention launch.
  * cap_desc, cap_bins and cap_units give the sizes of desc (entries of four
  * int32), bin_ptr and chunk_count / chunk_off, and are set by the caller.
- * B, Hkv and num_ctas are written by the planners (the host-side struct is
- * updated) and read by hpc_decode_attn / hpc_decode_combine, which launch
- * num_ctas CTAs and check B and Hkv against their own arguments.
+ * B, Hkv, num_ctas (the number of bins), persistent, min_tiles and
+ * max_pages (the planner's arguments) are written by the planners (the
+ * host-side struct is updated) and read by hpc_decode_attn /
+ * hpc_decode_combine, which check B and Hkv against their own arguments.
+ * The attention kernel of a persistent map re-derives each CTA's first
+ * descriptor from the sequence lengths so it can start before the map is
+ * complete; the map and the sequence lengths must describe the same batch.
+ * A persistent map (hpc_decode_plan) is drained by min(num_ctas, resident
+ * CTAs) persistent CTAs: CTA c takes bin c first and, when there are more
+ * bins than resident CTAs, pulls the remaining bins in order from the bin
+ * counter, so faster SMs take more bins.  A static map
+ * (hpc_decode_plan_static) launches one CTA per bin.
  */
 typedef struct {
     int32_t *desc;
@@ -97,7 +108,7 @@ typedef struct {
     int32_t *chunk_off;
     int32_t *meta;
     int32_t cap_desc, cap_bins, cap_units;
-    int32_t B, Hkv, num_ctas;
+    int32_t B, Hkv, num_ctas, persistent, min_tiles, max_pages;
 } hpc_task_map;
 
 /* Library version string (static storage). */
@@ -131,7 +142,10 @@ int64_t hpc_decode_static_capacity(int32_t B, int32_t Hkv, int32_t num_splits);
  * per-CTA budget max(ceil(T / num_ctas), min_tiles_per_cta, 1), walks tiles
  * head-major / batch-minor and fills bins in order, spilling into the next
  * bin when one is full.  Writes the whole task map (every bin_ptr entry,
- * every chunk_count/chunk_off entry, desc[0 .. num_desc), meta[0..3]).
+ * every chunk_count/chunk_off entry, desc[0 .. num_desc), meta[0..7]).
+ * num_ctas is the number of bins: the pages' choice is one bin per
+ * persistent CTA (hpc_decode_num_ctas); a small multiple of it lets the
+ * attention kernel balance uneven SM speeds by pulling bins dynamically.
  * The map is meant to be built once per decode step and reused by every
  * layer's hpc_decode_attn / hpc_decode_combine.
  *   d_seqlens          device [B] int32
@@ -139,7 +153,7 @@ int64_t hpc_decode_static_capacity(int32_t B, int32_t Hkv, int32_t num_splits);
  *   Hkv                >= 1
  *   max_pages_per_req  block-table row length; a seqlen above 64 * this is
  *                      clamped and flagged HPC_FLAG_BAD_SEQLEN
- *   num_ctas           >= 1, the attention grid size (see hpc_decode_num_ctas)
+ *   num_ctas           >= 1, the number of bins (see hpc_decode_num_ctas)
  *   min_tiles_per_cta  minimum-work floor (>= 0)
  *   map                cap_desc >= hpc_decode_desc_capacity(B, Hkv, num_ctas),
  *                      cap_bins >= num_ctas + 1 and cap_units >= B * Hkv,
@@ -192,6 +206,33 @@ hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *
                            hpc_stream_t stream);
 
 /*
+ * hpc_decode_attn with the combine step folded into the same persistent
+ * grid (the combine kernel's job, [vLLM] Compute and combine bullet, done
+ * without a second launch).  A unit whose chunk count is 1 writes its BF16
+ * output directly from the CTA that computed it; for a split unit every CTA
+ * writes its partial, then counts the chunk in d_unit_done[u] (device-scope
+ * fence before the atomic), and the CTA that brings the count to
+ * chunk_count[u] merges the unit's partials into d_out exactly as
+ * hpc_decode_combine does and resets the counter to 0 (chunks are counted,
+ * and units merged, at the end of each CTA's work).  Nothing waits on
+ * another CTA.  Requests with no live tokens get zero rows, as in
+ * hpc_decode_combine.
+ *   d_unit_done  device int32 [B * Hkv]; all zero before the call (clear it
+ *                once after allocating); every completed call leaves it zero.
+ *   d_out        device [B, Hq, 128] bf16
+ * Other arguments as in hpc_decode_attn; part_o / part_lse are still needed
+ * for the split units.
+ */
+hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                                   const void *d_v_cache, int32_t num_pages, float k_scale,
+                                   float v_scale, hpc_kv_dtype kv_dtype,
+                                   const int32_t *d_block_table, int32_t max_pages_per_req,
+                                   const int32_t *d_seqlens, int32_t B, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim, float sm_scale, const hpc_task_map *map,
+                                   float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
+                                   void *d_out, hpc_stream_t stream);
+
+/*
  * Combine ([vLLM] Compute and combine bullet: "reads the chunk count for each
  * (head, request) pair"; [SGL] 围绕Live KV Work的调度: merge under the correct
  * global softmax normalisation).  For every (r, hq), with unit
@@ -208,9 +249,10 @@ hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
 /*
  * One whole decode step of one layer on device buffers: hpc_decode_plan
  * (when num_splits == 0) or hpc_decode_plan_static (num_splits >= 1), then
- * hpc_decode_attn and hpc_decode_combine, all on `stream`.  Arguments as in
- * those calls.  In a real model the plan is built once per step and shared
- * by all layers; this call rebuilds it every time.
+ * either hpc_decode_attn_combine (d_unit_done != NULL) or hpc_decode_attn
+ * followed by hpc_decode_combine (d_unit_done == NULL), all on `stream`.
+ * Arguments as in those calls.  In a real model the plan is built once per
+ * step and shared by all layers; this call rebuilds it every time.
  */
 hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *d_k_cache,
                            const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
@@ -218,8 +260,8 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
                            int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
                            int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                            int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
-                           hpc_task_map *map, float *d_part_o, float *d_part_lse, void *d_out,
-                           hpc_stream_t stream);
+                           hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                           int32_t *d_unit_done, void *d_out, hpc_stream_t stream);
 
 /*
  * hpc_decode_step with the per-step inputs and the output in host memory
@@ -238,7 +280,7 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
                                 int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                                 int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
                                 hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                                hpc_stream_t stream);
+                                int32_t *d_unit_done, hpc_stream_t stream);
 
 /*
  * Size of the scratch array compiled into the library for

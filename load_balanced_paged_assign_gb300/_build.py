@@ -45,12 +45,17 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compile the library (to `out`, default the package's libhpcdecode.so).
+
+    `defines` are extra -D settings, e.g. the pipeline shape of the attention
+    kernels (HPC_BF16_STAGES, HPC_BF16_TPS, HPC_FP8_STAGES, HPC_FP8_TPS)."""
+    target = out or LIB_PATH
+    if not force and not defines and out is None and not is_stale():
         return LIB_PATH
     nvcc = _nvcc()
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                    "--expt-relaxed-constexpr"]
+                    "--expt-relaxed-constexpr"] + [f"-D{d}" for d in defines]
     with tempfile.TemporaryDirectory(prefix="hpcdecode_build_") as tmp:
         def compile_one(src):
             obj = os.path.join(tmp, os.path.basename(src) + ".o")
@@ -69,11 +74,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr}")
-        staged = LIB_PATH + f".{os.getpid()}.tmp"
+        staged = target + f".{os.getpid()}.tmp"
         shutil.copyfile(out_tmp, staged)
-        os.replace(staged, LIB_PATH)
-    return LIB_PATH
+        os.replace(staged, target)
+    return target
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    import argparse
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--define", "-D", action="append", default=[])
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args()
+    print(build(force=True, verbose=True, defines=a.define, out=a.out))

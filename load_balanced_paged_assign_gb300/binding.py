@@ -24,7 +24,7 @@ HEAD_DIM, PAGE_SIZE, MAX_GROUP = 128, 64, 8
 EXPORTS = (
     "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
     "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
-    "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
+    "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
     "hpc_decode_step_noalloc",
 )
 
@@ -42,6 +42,8 @@ class hpc_task_map(ctypes.Structure):
         ("meta", ctypes.c_void_p),
         ("cap_desc", ctypes.c_int32), ("cap_bins", ctypes.c_int32), ("cap_units", ctypes.c_int32),
         ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("persistent", ctypes.c_int32), ("min_tiles", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32),
     ]
 
 
@@ -49,7 +51,9 @@ _LIB = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The in-tree library, or the file named by HPC_DECODE_LIB (another build
+    of the same sources, e.g. with a different pipeline shape)."""
+    return os.environ.get("HPC_DECODE_LIB") or _build.LIB_PATH
 
 
 def lib():
@@ -57,7 +61,7 @@ def lib():
     global _LIB
     if _LIB is not None:
         return _LIB
-    path = _build.LIB_PATH
+    path = library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it first "
                            "(python -c 'import __graft_entry__ as g; g.build()')")
@@ -74,13 +78,16 @@ def lib():
         "hpc_decode_plan_static": (ctypes.c_int, [vp, i32, i32, i32, i32, tm, vp]),
         "hpc_decode_attn": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp, i32,
                                            vp, i32, i32, i32, i32, f32, tm, vp, vp, vp]),
+        "hpc_decode_attn_combine": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
+                                                   vp, i32, vp, i32, i32, i32, i32, f32, tm, vp,
+                                                   vp, vp, vp, vp]),
         "hpc_decode_combine": (ctypes.c_int, [vp, vp, tm, i32, i32, i32, i32, vp, vp]),
         "hpc_decode_step": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp, i32,
                                            vp, i32, i32, i32, i32, f32, i32, i32, i32, tm, vp,
-                                           vp, vp, vp]),
+                                           vp, vp, vp, vp]),
         "hpc_decode_step_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 i32, f32, f32, ctypes.c_int, i32, i32, i32, i32,
-                                                i32, f32, i32, i32, i32, tm, vp, vp, vp]),
+                                                i32, f32, i32, i32, i32, tm, vp, vp, vp, vp]),
         "hpc_decode_read_meta": (ctypes.c_int, [tm, ctypes.POINTER(ctypes.c_int32), vp]),
         "hpc_decode_step_noalloc": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
                                                    vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
@@ -133,10 +140,10 @@ class TaskMap:
         units = max(B * Hkv, 1)
         self.chunk_count = torch.zeros(units, dtype=torch.int32, device=dev)
         self.chunk_off = torch.zeros(units, dtype=torch.int32, device=dev)
-        self.meta = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.meta = torch.zeros(8, dtype=torch.int32, device=dev)
         self.c = hpc_task_map(_ptr(self.desc), _ptr(self.bin_ptr), _ptr(self.chunk_count),
                               _ptr(self.chunk_off), _ptr(self.meta), cap_desc, cap_bins, units, 0,
-                              0, 0)
+                              0, 0, 0, 0, 0)
 
     @classmethod
     def dynamic(cls, B: int, Hkv: int, num_ctas: int, device="cuda"):
@@ -213,6 +220,17 @@ def hpc_decode_attn(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
         _stream(stream)))
 
 
+def hpc_decode_attn_combine(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens,
+                            Hq, Hkv, sm_scale, tmap: TaskMap, part_o, part_lse, unit_done, out,
+                            stream=None):
+    _check("hpc_decode_attn_combine", lib().hpc_decode_attn_combine(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, float(sm_scale), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse),
+        _ptr(unit_done), _ptr(out), _stream(stream)))
+
+
 def hpc_decode_combine(part_o, part_lse, tmap: TaskMap, B, Hq, Hkv, out, stream=None):
     _check("hpc_decode_combine", lib().hpc_decode_combine(
         _ptr(part_o), _ptr(part_lse), ctypes.byref(tmap.c), int(B), int(Hq), int(Hkv), HEAD_DIM,
@@ -221,26 +239,29 @@ def hpc_decode_combine(part_o, part_lse, tmap: TaskMap, B, Hq, Hkv, out, stream=
 
 def hpc_decode_step(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens, Hq,
                     Hkv, sm_scale, num_ctas, min_tiles_per_cta, num_splits, tmap: TaskMap, part_o,
-                    part_lse, out, stream=None):
+                    part_lse, out, unit_done=None, stream=None):
+    """unit_done given: fused attention + combine; None: separate combine kernel."""
     _check("hpc_decode_step", lib().hpc_decode_step(
         _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
         float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
         int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
         HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta), int(num_splits),
-        ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(out), _stream(stream)))
+        ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(unit_done), _ptr(out),
+        _stream(stream)))
 
 
 def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d_q_scale,
                          d_seqlens, d_block_table, d_out, k_cache, v_cache, k_scale, v_scale, Hq,
                          Hkv, sm_scale, num_ctas, min_tiles_per_cta, num_splits, tmap: TaskMap,
-                         part_o, part_lse, stream=None):
+                         part_o, part_lse, unit_done=None, stream=None):
     _check("hpc_decode_step_host", lib().hpc_decode_step_host(
         _ptr(h_q), _ptr(h_q_scale), _ptr(h_seqlens), _ptr(h_block_table), _ptr(h_out), _ptr(d_q),
         _ptr(d_q_scale), _ptr(d_seqlens), _ptr(d_block_table), _ptr(d_out), _ptr(k_cache),
         _ptr(v_cache), int(k_cache.shape[0]), float(k_scale), float(v_scale),
         kv_dtype_of(k_cache), int(h_block_table.shape[1]), int(h_seqlens.numel()), int(Hq),
         int(Hkv), HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta),
-        int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _stream(stream)))
+        int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(unit_done),
+        _stream(stream)))
 
 
 def hpc_decode_read_meta(tmap: TaskMap, stream=None) -> list:
@@ -280,3 +301,5 @@ class Workspace:
         self.part_o = torch.empty((cap, G, HEAD_DIM), dtype=torch.float32, device=dev)
         self.part_lse = torch.empty((cap, G), dtype=torch.float32, device=dev)
         self.out = torch.empty((max(B, 1), Hq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        # chunk counters of the fused combine: zero once, left zero by every launch
+        self.unit_done = torch.zeros(max(B * Hkv, 1), dtype=torch.int32, device=dev)

@@ -4,6 +4,7 @@
 // hpc_decode_read_meta.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -102,10 +103,105 @@ hpc_status make_cache_map(CUtensorMap *m, const void *base, int32_t num_pages, i
     return r == CUDA_SUCCESS ? HPC_OK : HPC_ERR_CUDA;
 }
 
+// Resident CTAs of the attention kernel per device and KV dtype (cached).
+std::atomic<int> g_capacity[kMaxDevices][2];
+
+int resident_ctas(const AttnConfig &cfg, int which) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    int c = g_capacity[dev][which].load();
+    if (c > 0) return c;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kernel, cfg.threads,
+                                                      cfg.smem_bytes) != cudaSuccess ||
+        per_sm < 1)
+        return -1;
+    c = sms * per_sm;
+    g_capacity[dev][which].store(c);
+    return c;
+}
+
 const AttnConfig &config_for(hpc_kv_dtype dt) {
     static const AttnConfig bf16 = attn_config_bf16();
     static const AttnConfig fp8 = attn_config_fp8();
     return dt == HPC_KV_FP8_E4M3 ? fp8 : bf16;
+}
+
+// Shared body of hpc_decode_attn (unit_done == out == nullptr: partials only)
+// and hpc_decode_attn_combine (fused combine).
+hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                            const void *d_v_cache, int32_t num_pages, float k_scale,
+                            float v_scale, hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                            int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                            int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                            const hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                            int32_t *d_unit_done, void *d_out, hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
+    if (st != HPC_OK) return st;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (num_pages <= 0 || !d_k_cache || !d_v_cache || !d_part_o || !d_part_lse)
+        return HPC_ERR_ARG;
+    if (B > 0 && (!d_q || !d_block_table || !d_seqlens)) return HPC_ERR_ARG;
+    if (fp8 && B > 0 && !d_q_scale) return HPC_ERR_ARG;
+    if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) ||
+        !aligned16(d_part_o))
+        return HPC_ERR_ARG;
+    if (!std::isfinite(sm_scale) || (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale))))
+        return HPC_ERR_ARG;
+    st = check_map(map, false);
+    if (st != HPC_OK) return st;
+    if (map->B != B || map->Hkv != Hkv || map->num_ctas < 1 || map->num_ctas >= map->cap_bins)
+        return HPC_ERR_ARG;
+
+    CUtensorMap tk, tv;
+    st = make_cache_map(&tk, d_k_cache, num_pages, Hkv, fp8);
+    if (st == HPC_OK) st = make_cache_map(&tv, d_v_cache, num_pages, Hkv, fp8);
+    if (st != HPC_OK) return st;
+
+    AttnParams p;
+    p.bin_ptr = map->bin_ptr;
+    p.desc = reinterpret_cast<const int4 *>(map->desc);
+    p.chunk_count = map->chunk_count;
+    p.chunk_off = map->chunk_off;
+    p.unit_done = d_unit_done;
+    p.out = d_out;
+    p.seqlens = d_seqlens;
+    p.block_table = d_block_table;
+    p.q = d_q;
+    p.q_scale = d_q_scale;
+    p.part_o = d_part_o;
+    p.part_lse = d_part_lse;
+    p.meta = map->meta;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.max_pages = max_pages_per_req;
+    p.num_pages = num_pages;
+    p.score_scale = sm_scale * kLog2eF * (fp8 ? k_scale : 1.f);
+    p.v_scale = fp8 ? v_scale : 1.f;
+
+    const AttnConfig &cfg = config_for(kv_dtype);
+    cudaError_t e = prepare_kernel(cfg, fp8 ? 1 : 0);
+    if (e != cudaSuccess) return HPC_ERR_CUDA;
+    int grid = map->num_ctas;  // static map: one CTA per bin
+    if (map->persistent) {     // persistent: resident CTAs, extra bins pulled dynamically
+        const int cap = resident_ctas(cfg, fp8 ? 1 : 0);
+        if (cap < 1) return HPC_ERR_CUDA;
+        grid = std::min(grid, cap);
+    }
+    p.num_bins = map->num_ctas;
+    p.bin_counter = map->meta + 4;
+    p.min_tiles = map->min_tiles;
+    // the first descriptor is derived in-kernel only for a load-balanced map
+    // planned against this very block-table shape
+    p.fly = map->persistent && map->max_pages == max_pages_per_req ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = fp8 ? launch_attn_fp8(tk, tv, p, grid, s) : launch_attn_bf16(tk, tv, p, grid, s);
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -144,7 +240,7 @@ int32_t hpc_decode_num_ctas(int32_t device, hpc_kv_dtype kv_dtype) {
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = prepare_kernel(cfg, kv_dtype == HPC_KV_FP8_E4M3 ? 1 : 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kernel, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kernel, cfg.threads,
                                                           cfg.smem_bytes);
     if (device != prev) cudaSetDevice(prev);
     if (e != cudaSuccess || per_sm < 1) return HPC_ERR_CUDA;
@@ -169,6 +265,9 @@ hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
     m.B = B;
     m.Hkv = Hkv;
     m.num_ctas = num_ctas;
+    m.persistent = 1;
+    m.min_tiles = min_tiles_per_cta;
+    m.max_pages = max_pages_per_req;
     st = cuda_status(launch_assign(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
                                    min_tiles_per_cta, m, static_cast<cudaStream_t>(stream)));
     if (st == HPC_OK) *map = m;
@@ -193,6 +292,9 @@ hpc_status hpc_decode_plan_static(const int32_t *d_seqlens, int32_t B, int32_t H
     m.B = B;
     m.Hkv = Hkv;
     m.num_ctas = (int32_t)bins;
+    m.persistent = 0;
+    m.min_tiles = num_splits;
+    m.max_pages = max_pages_per_req;
     st = cuda_status(launch_static_plan(d_seqlens, B, Hkv, max_pages_per_req, num_splits, m,
                                         static_cast<cudaStream_t>(stream)));
     if (st == HPC_OK) *map = m;
@@ -206,55 +308,28 @@ hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *
                            int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                            const hpc_task_map *map, float *d_part_o, float *d_part_lse,
                            hpc_stream_t stream) {
-    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
-    if (st != HPC_OK) return st;
-    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
-    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
-    if (num_pages <= 0 || !d_k_cache || !d_v_cache || !d_part_o || !d_part_lse)
-        return HPC_ERR_ARG;
-    if (B > 0 && (!d_q || !d_block_table || !d_seqlens)) return HPC_ERR_ARG;
-    if (fp8 && B > 0 && !d_q_scale) return HPC_ERR_ARG;
-    if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) ||
-        !aligned16(d_part_o))
-        return HPC_ERR_ARG;
-    if (!std::isfinite(sm_scale) || (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale))))
-        return HPC_ERR_ARG;
-    st = check_map(map, false);
-    if (st != HPC_OK) return st;
-    if (map->B != B || map->Hkv != Hkv || map->num_ctas < 1 || map->num_ctas >= map->cap_bins)
-        return HPC_ERR_ARG;
+    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                            head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr,
+                            stream);
+}
 
-    CUtensorMap tk, tv;
-    st = make_cache_map(&tk, d_k_cache, num_pages, Hkv, fp8);
-    if (st == HPC_OK) st = make_cache_map(&tv, d_v_cache, num_pages, Hkv, fp8);
-    if (st != HPC_OK) return st;
-
-    AttnParams p;
-    p.bin_ptr = map->bin_ptr;
-    p.desc = reinterpret_cast<const int4 *>(map->desc);
-    p.seqlens = d_seqlens;
-    p.block_table = d_block_table;
-    p.q = d_q;
-    p.q_scale = d_q_scale;
-    p.part_o = d_part_o;
-    p.part_lse = d_part_lse;
-    p.meta = map->meta;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.G = Hq / Hkv;
-    p.max_pages = max_pages_per_req;
-    p.num_pages = num_pages;
-    p.score_scale = sm_scale * kLog2eF * (fp8 ? k_scale : 1.f);
-    p.v_scale = fp8 ? v_scale : 1.f;
-
-    const AttnConfig &cfg = config_for(kv_dtype);
-    cudaError_t e = prepare_kernel(cfg, fp8 ? 1 : 0);
-    if (e != cudaSuccess) return HPC_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = fp8 ? launch_attn_fp8(tk, tv, p, map->num_ctas, s)
-            : launch_attn_bf16(tk, tv, p, map->num_ctas, s);
-    return cuda_status(e);
+hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                                   const void *d_v_cache, int32_t num_pages, float k_scale,
+                                   float v_scale, hpc_kv_dtype kv_dtype,
+                                   const int32_t *d_block_table, int32_t max_pages_per_req,
+                                   const int32_t *d_seqlens, int32_t B, int32_t Hq, int32_t Hkv,
+                                   int32_t head_dim, float sm_scale, const hpc_task_map *map,
+                                   float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
+                                   void *d_out, hpc_stream_t stream) {
+    if (B > 0 && (!d_unit_done || !d_out)) return HPC_ERR_ARG;
+    if (!aligned16(d_out)) return HPC_ERR_ARG;
+    if (!map || !map->chunk_count || !map->chunk_off) return HPC_ERR_ARG;
+    if ((int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
+    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                            head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
+                            stream);
 }
 
 hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
@@ -277,8 +352,8 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
                            int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
                            int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                            int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
-                           hpc_task_map *map, float *d_part_o, float *d_part_lse, void *d_out,
-                           hpc_stream_t stream) {
+                           hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                           int32_t *d_unit_done, void *d_out, hpc_stream_t stream) {
     hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
     if (st != HPC_OK) return st;
     if (num_splits < 0) return HPC_ERR_ARG;
@@ -287,6 +362,11 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
                          : hpc_decode_plan_static(d_seqlens, B, Hkv, max_pages_per_req,
                                                   num_splits, map, stream);
     if (st != HPC_OK) return st;
+    if (d_unit_done)  // fused: the attention grid also performs the combine
+        return hpc_decode_attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale,
+                                       v_scale, kv_dtype, d_block_table, max_pages_per_req,
+                                       d_seqlens, B, Hq, Hkv, head_dim, sm_scale, map, d_part_o,
+                                       d_part_lse, d_unit_done, d_out, stream);
     st = hpc_decode_attn(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                          kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                          head_dim, sm_scale, map, d_part_o, d_part_lse, stream);
@@ -303,7 +383,7 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
                                 int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                                 int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
                                 hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                                hpc_stream_t stream) {
+                                int32_t *d_unit_done, hpc_stream_t stream) {
     hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
     if (st != HPC_OK) return st;
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
@@ -332,7 +412,7 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
     st = hpc_decode_step(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                          kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                          head_dim, sm_scale, num_ctas, min_tiles_per_cta, num_splits, map,
-                         d_part_o, d_part_lse, d_out, stream);
+                         d_part_o, d_part_lse, d_unit_done, d_out, stream);
     if (st != HPC_OK) return st;
     if (B > 0) e = cudaMemcpyAsync(h_out, d_out, out_bytes, cudaMemcpyDeviceToHost, s);
     return cuda_status(e);

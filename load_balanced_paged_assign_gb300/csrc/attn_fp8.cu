@@ -3,19 +3,38 @@
 
 namespace hpc {
 
-// 8 stages x (8 KB K + 8 KB V + 1 KB Q): about 155 KB, one CTA per SM.
-constexpr int kStagesFp8 = 8;
+// 4 stages x 2 tiles x (8 KB K + 8 KB V) + Q: about 150 KB, one CTA per SM; two
+// tiles per stage give 8 consumer warps, which FP8 needs to hide its per-tile latency.
+#ifndef HPC_FP8_STAGES
+#define HPC_FP8_STAGES 4
+#endif
+#ifndef HPC_FP8_TPS
+#define HPC_FP8_TPS 2
+#endif
+constexpr int kStagesFp8 = HPC_FP8_STAGES;  // pipeline depth (build-time tunable)
+constexpr int kTpsFp8 = HPC_FP8_TPS;        // tiles per stage: 1 or 2
+using TraitsFp8 = AttnTraits<true, kStagesFp8, kTpsFp8>;
 
 AttnConfig attn_config_fp8() {
-    return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8>),
-            AttnTraits<true, kStagesFp8>::kSmemBytes, kStagesFp8};
+    return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8, kTpsFp8>),
+            TraitsFp8::kSmemBytes, TraitsFp8::kThreads};
 }
 
+// Launched as a programmatic dependent of the previous kernel in the stream
+// (the assign kernel): its prologue overlaps that kernel's tail.
 cudaError_t launch_attn_fp8(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                            int grid, cudaStream_t s) {
-    constexpr int smem = AttnTraits<true, kStagesFp8>::kSmemBytes;
-    attn_kernel<true, kStagesFp8><<<grid, kThreads, smem, s>>>(tk, tv, p);
-    return cudaGetLastError();
+                             int grid, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TraitsFp8::kThreads);
+    cfg.dynamicSmemBytes = TraitsFp8::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8, kTpsFp8>, tk, tv, p);
 }
 
 }  // namespace hpc

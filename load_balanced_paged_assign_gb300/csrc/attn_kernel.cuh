@@ -1,33 +1,52 @@
 // Persistent load-balanced paged GQA decode attention (HPC-Ops vLLM post,
 // "Compute and combine" bullet; SGLang post, 围绕Live KV Work的调度,
-// execution paragraph): CTA c drains bin c of the task map.  For every
-// descriptor (h, r, tb, te) it streams KV pages block_table[r][tb .. te) of
-// KV head h and writes, for the GQA group of h, the normalised partial
-// output and its log-sum-exp into split-buffer slot = descriptor index.
+// execution paragraph): the persistent CTAs drain the bins of the task map.
+// For every descriptor (h, r, tb, te) a CTA streams KV pages
+// block_table[r][tb .. te) of KV head h and produces, for the GQA group of
+// h, the normalised partial output and its log-sum-exp (split-buffer slot =
+// descriptor index).  In the fused mode it also performs the combine step: a
+// unit with one chunk writes its BF16 output directly, and for a split unit
+// the CTA that counts the unit's last chunk merges all of its partials.
 //
 // GB300 design (the pages' Hopper kernel is not followed):
-//  * warp 0 is a producer: one lane walks the whole bin as a flat stream of
-//    tiles and issues one TMA tile load per 64-token page of K and of V into
-//    a STAGES-deep ring of shared-memory stages (mbarrier full/empty pairs),
-//    so loads keep flowing across descriptor boundaries.  Q (and the FP8
-//    q-scales) ride in the stage holding a descriptor's first tile.  After
-//    the last tile it posts a terminator stage.
-//  * warps 1..4 are consumers; warp w owns tokens 16w .. 16w + 15 of every
-//    tile and keeps its own online-softmax state; the four states are merged
-//    through shared memory at the end of each descriptor.
-//  * the contractions run on mma.sync with the operands swapped so the
-//    GQA group is the N = 8 side:  S^T[tok, head] = K[tok, :] . Q^T and
+//  * warp 0 is a producer: one lane walks the CTA's bins as a flat stream of
+//    tiles and issues TMA tile loads (one per 64-token page of K and of V)
+//    into a STAGES-deep ring of shared-memory stages guarded by full/empty
+//    mbarriers, so loads keep flowing across descriptor boundaries.  A stage
+//    holds TPS tiles of one descriptor.  Q (and the FP8 q-scales) ride in the
+//    stage holding a descriptor's first tile.  After the last tile the
+//    producer posts a terminator stage.
+//  * 4 * TPS consumer warps (warps 2 ..): warp w owns tokens 16 (w % 4) ..
+//    + 15 of tile w / 4 of every stage and keeps its own online-softmax
+//    state.  At a descriptor's end each consumer hands its state to a
+//    double-buffered shared-memory slot and goes straight on with the next
+//    stage; it never waits for the merge.
+//  * warp 1 is a combiner: it merges the consumers' states of each finished
+//    descriptor, writes the BF16 output or the partial and its LSE, and counts
+//    the chunks of split units at once, so no consumer ever waits on that
+//    bookkeeping.  The merges of split units whose last chunk this CTA counts
+//    run at the end, spread over all warps.
+//  * contractions run on mma.sync with the operands swapped so the GQA group
+//    is the N = 8 side:  S^T[tok, head] = K[tok, :] . Q^T and
 //    O^T[dim, head] += V^T[dim, tok] . P^T[tok, head].  P^T's B fragment is
-//    the S^T accumulator transposed in registers with movmatrix, so no
-//    shared-memory round trip and no padding of the 8-head group to M = 16.
+//    the S^T accumulator transposed in registers with movmatrix, so there is
+//    no shared-memory round trip and no padding of the 8-head group to M = 16.
 //  * BF16: K via ldmatrix, V via ldmatrix.trans, bf16 MMAs.
 //    FP8: Q.K^T on e4m3 MMAs (m16n8k32) straight from the FP8 Q and cache;
 //    V is widened exactly to f16 in registers (byte permutes + cvt) with the
 //    output dims permuted so each lane needs one 16-byte row segment per
 //    token; P stays f16 (never quantised).
 //  * tiles land with the 128-byte swizzle; every ldmatrix / 16-byte read
-//    below touches 8 distinct 16-byte bank groups.
+//    touches 8 distinct 16-byte bank groups, and the state hand-off is
+//    lane-major, so it is conflict-free too.
+//  * the kernel is launched as a programmatic dependent of the assign kernel:
+//    it sets up its barriers, prefetches the block table into L2, derives its
+//    first descriptor from the sequence lengths and starts streaming while
+//    the assign kernel may still be running; only the producer waits for the
+//    task map, when it first needs it.
 #pragma once
+
+#include <cuda_bf16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -35,15 +54,34 @@
 namespace hpc {
 
 struct StageInfo {
-    int kv_head, req, tile, flags;
-    int seqlen, desc_idx, pad0, pad1;
+    int kv_head, req, tile0, ntiles;  // tiles tile0 .. tile0 + ntiles - 1 of request req
+    int flags, seqlen, desc_idx, count;  // count: chunks of the unit
+    int chunk_off, pad0, pad1, pad2;
     float qscale[kMaxGroup];
+    int pad3[4];
 };
-static_assert(sizeof(StageInfo) == 64, "StageInfo layout");
+static_assert(sizeof(StageInfo) == 96, "StageInfo layout");
+
+// The fields of a descriptor the combine step needs.
+struct DescInfo {
+    int req, kv_head, desc_idx, count, chunk_off;
+};
+
+struct SlotInfo {  // what a consumer hand-off slot holds besides the states
+    DescInfo di;
+    int flags, pad0, pad1;
+};
+static_assert(sizeof(SlotInfo) == 32, "SlotInfo layout");
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kCombSlots = 2;   // hand-off slots (double buffer)
+constexpr int kStateRegs = 36;  // per lane: 32 accumulators, m0, m1, l0, l1
+constexpr int kMaxLast = 16;    // split units whose merge this CTA owes, held at once
+constexpr int kStageStride = kHeadDim + 4;  // floats per head row of the combiner's staging
+constexpr int kFlyMaxBatch = 1024;  // largest batch whose first descriptor is derived in-kernel
 
 // Warp-uniform bounded wait: lane 0 polls (so all lanes agree on the
 // outcome), then every lane re-observes the completed phase for its own
@@ -56,235 +94,480 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <bool FP8, int STAGES>
+template <bool FP8, int STAGES, int TPS>
 struct AttnTraits {
+    static constexpr int kConsumers = kConsumerWarps * TPS;          // consumer warps
+    static constexpr int kThreads = 32 * (2 + kConsumers);           // + producer, combiner
     static constexpr int kElem = FP8 ? 1 : 2;
-    static constexpr int kTileBytes = kTile * kHeadDim * kElem;   // one K or V page of one head
-    static constexpr int kHalfBytes = kTile * 64 * 2;             // BF16: one 64-dim half
-    static constexpr int kQBytes = kMaxGroup * kHeadDim * kElem;  // Q slot per stage
-    static constexpr int kCombStride = kHeadDim + 4;              // floats per head row
+    static constexpr int kTileBytes = kTile * kHeadDim * kElem;     // one K or V page, one head
+    static constexpr int kHalfBytes = kTile * 64 * 2;               // BF16: one 64-dim half
+    static constexpr int kStageKV = TPS * kTileBytes;               // K (or V) bytes per stage
+    static constexpr int kQBytes = kMaxGroup * kHeadDim * kElem;    // Q slot per stage
+    static constexpr int kSlotFloats = kConsumers * kStateRegs * 32;  // one hand-off slot
     static constexpr int kOffK = 0;
-    static constexpr int kOffV = kOffK + STAGES * kTileBytes;
-    static constexpr int kOffQ = kOffV + STAGES * kTileBytes;
+    static constexpr int kOffV = kOffK + STAGES * kStageKV;
+    static constexpr int kOffQ = kOffV + STAGES * kStageKV;
     static constexpr int kOffInfo = kOffQ + STAGES * kQBytes;
-    static constexpr int kOffBar = kOffInfo + STAGES * (int)sizeof(StageInfo);
-    static constexpr int kOffAbort = kOffBar + (2 * STAGES + 2) * 8;  // + epilogue pair
-    static constexpr int kOffComb = (kOffAbort + 16 + 15) / 16 * 16;
-    static constexpr int kOffStat = kOffComb + kConsumerWarps * kMaxGroup * kCombStride * 4;
-    static constexpr int kBytes = kOffStat + 2 * kConsumerWarps * kMaxGroup * 4;
+    static constexpr int kOffComb = kOffInfo + STAGES * (int)sizeof(StageInfo);
+    static constexpr int kOffStage = kOffComb + kCombSlots * kSlotFloats * 4;
+    static constexpr int kOffSlotInfo = kOffStage + kMaxGroup * kStageStride * 4;
+    static constexpr int kOffLast = kOffSlotInfo + kCombSlots * (int)sizeof(SlotInfo);
+    static constexpr int kOffBar = kOffLast + (kMaxLast + 1) * (int)sizeof(SlotInfo);
+    // full[STAGES], empty[STAGES], slot full[2], slot empty[2], end rendezvous
+    static constexpr int kNumBars = 2 * STAGES + 2 * kCombSlots + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // abort word
+    static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;  // slack to align the base to 1024 B
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <bool FP8, int STAGES>
+// ------------------------------------------------------------------ producer
+// Shared state of the producer warp.
+struct ProducerState {
+    uint32_t it;          // stages issued so far
+    bool waited;          // grid_dependency_wait done: the task map may be read
+    unsigned late_flags;  // device error bits, OR-ed into meta[3] after the wait
+};
+
+__device__ __forceinline__ void wait_for_map(ProducerState &ps) {
+    if (!ps.waited) {
+        grid_dependency_wait();
+        ps.waited = true;
+    }
+}
+
+// First descriptor of bin c, from the sequence lengths alone (the closed form
+// of the assign kernel: n_r = ceil(L_r / 64) with the same clamping, T =
+// Hkv * sum n_r, budget = max(ceil(T / bins), floor, 1), bin c = global tiles
+// [c * budget, ...), units head-major).  Returns false when the batch is too
+// large to scan here; te == tb means the bin is empty.
+__device__ __forceinline__ bool first_descriptor(const AttnParams &p, int c, int &h, int &r,
+                                                 int &tb, int &te) {
+    if (p.B > kFlyMaxBatch) return false;
+    const int lane = threadIdx.x & 31, cap = p.max_pages * kTile;
+    int N = 0;
+    for (int base = 0; base < p.B; base += 32) {
+        const int rr = base + lane;
+        int L = rr < p.B ? p.seqlens[rr] : 0;
+        L = L < 0 ? 0 : min(L, cap);
+        N += __reduce_add_sync(kFullMask, (L + kTile - 1) / kTile);
+    }
+    const long long T = (long long)p.Hkv * N;
+    const int budget = (int)max((T + p.num_bins - 1) / p.num_bins, (long long)max(p.min_tiles, 1));
+    const long long t = (long long)c * budget;
+    h = r = tb = te = 0;
+    if (t >= T) return true;  // an empty bin
+    h = (int)(t / N);
+    const int tl = (int)(t - (long long)h * N);
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+        const int rr = base + lane;
+        int L = rr < p.B ? p.seqlens[rr] : 0;
+        L = L < 0 ? 0 : min(L, cap);
+        const int n = (L + kTile - 1) / kTile;
+        int incl = n;  // inclusive prefix of n over this chunk
+#pragma unroll
+        for (int o_ = 1; o_ < 32; o_ <<= 1) {
+            const int y = __shfl_up_sync(kFullMask, incl, o_);
+            if (lane >= o_) incl += y;
+        }
+        const unsigned hit = __ballot_sync(kFullMask, rr < p.B && carry + incl > tl);
+        if (hit) {  // the request holding global tile t
+            const int l = __ffs(hit) - 1;
+            const int start = carry + __shfl_sync(kFullMask, incl - n, l);
+            const int nr = __shfl_sync(kFullMask, n, l);
+            r = base + l;
+            tb = tl - start;
+            te = tb + (int)min((long long)(nr - tb), T - t < budget ? T - t : (long long)budget);
+            return true;
+        }
+        carry += __shfl_sync(kFullMask, incl, 31);
+    }
+    return true;  // unreachable for a consistent batch
+}
+
+// Streams one descriptor (h, r, tb, te) through the stage ring.  desc_idx is
+// its index in the task map, or -1 when it is the first descriptor of bin
+// `bin` derived before the map could be read.  Returns false after a timeout.
+template <bool FP8, int STAGES, int TPS>
+__device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
+                                            const AttnParams &p, uint8_t *smem, int h, int r,
+                                            int tb, int te, int desc_idx, int bin,
+                                            ProducerState &ps, uint64_t policy,
+                                            volatile int *abort) {
+    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    const int lane = threadIdx.x & 31;
+    StageInfo *info = reinterpret_cast<StageInfo *>(smem + Tr::kOffInfo);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
+    uint64_t *empty = full + STAGES;
+    const uint32_t q_bytes = (uint32_t)(p.G * kHeadDim * Tr::kElem);
+    if (tb >= te) return true;  // empty split of the static schedule
+    const int L = p.seqlens[r];
+    const int u = h * p.B + r;
+    float qs = 1.f;
+    if (FP8 && lane < p.G) qs = p.q_scale[(size_t)r * p.Hq + h * p.G + lane];
+    float qsg[kMaxGroup];
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
+    const int32_t *bt_row = p.block_table + (size_t)r * p.max_pages;
+    const uint8_t *q_src = static_cast<const uint8_t *>(p.q) +
+                           ((size_t)r * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
+
+    for (int t0 = tb; t0 < te; t0 += 32) {  // 32 block-table entries at a time
+        const int nt = min(32, te - t0);
+        int page = 0;
+        if (lane < nt) {
+            page = bt_row[t0 + lane];
+            if (page < 0 || page >= p.num_pages) {
+                ps.late_flags |= HPC_FLAG_BAD_PAGE;
+                page = 0;  // stay inside the cache; the result is flagged as invalid
+            }
+        }
+        for (int k = 0; k < nt; k += TPS) {
+            const int ns = min(TPS, nt - k);  // tiles in this stage
+            int pg[TPS];
+#pragma unroll
+            for (int s = 0; s < TPS; ++s) pg[s] = __shfl_sync(kFullMask, page, min(k + s, 31));
+            const bool last_stage = t0 + k + ns == te;
+            int idx = desc_idx, count = 0, chunk_off = 0;
+            if (last_stage) {  // the combine step needs the unit's chunk layout
+                wait_for_map(ps);
+                if (idx < 0) idx = p.bin_ptr[bin];
+                if (p.chunk_count) {
+                    count = p.chunk_count[u];
+                    chunk_off = p.chunk_off[u];
+                }
+            }
+            const int stage = ps.it % STAGES;
+            const uint32_t phase = (ps.it / STAGES) & 1u;
+            if (!warp_wait(&empty[stage], phase ^ 1u, abort)) return false;
+            if (lane == 0) {
+                const int t = t0 + k;
+                const bool first = t == tb;
+                StageInfo &si = info[stage];
+                si.kv_head = h;
+                si.req = r;
+                si.tile0 = t;
+                si.ntiles = ns;
+                si.flags = (first ? kFirst : 0) | (last_stage ? kLast : 0);
+                si.seqlen = L;
+                si.desc_idx = idx;
+                si.count = count;
+                si.chunk_off = chunk_off;
+#pragma unroll
+                for (int g = 0; g < kMaxGroup; ++g) si.qscale[g] = qsg[g];
+                mbar_arrive_expect_tx(&full[stage], 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u));
+#pragma unroll
+                for (int s = 0; s < TPS; ++s) {
+                    if (s >= ns) break;
+                    uint8_t *sk = smem + Tr::kOffK + stage * Tr::kStageKV + s * Tr::kTileBytes;
+                    uint8_t *sv = smem + Tr::kOffV + stage * Tr::kStageKV + s * Tr::kTileBytes;
+                    if (FP8) {
+                        tma_load_4d(sk, tmap_k, &full[stage], 0, h, 0, pg[s], policy);
+                        tma_load_4d(sv, tmap_v, &full[stage], 0, h, 0, pg[s], policy);
+                    } else {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            tma_load_5d(sk + half * Tr::kHalfBytes, tmap_k, &full[stage], 0, half,
+                                        h, 0, pg[s], policy);
+                            tma_load_5d(sv + half * Tr::kHalfBytes, tmap_v, &full[stage], 0, half,
+                                        h, 0, pg[s], policy);
+                        }
+                    }
+                }
+                if (first)
+                    bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes, q_src, q_bytes, &full[stage]);
+            }
+            __syncwarp();
+            ++ps.it;
+        }
+    }
+    return true;
+}
+
+template <bool FP8, int STAGES, int TPS>
 __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
-                                              const AttnParams &p, uint8_t *smem, int d_begin,
-                                              int d_end, volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES>;
+                                              const AttnParams &p, uint8_t *smem,
+                                              volatile int *abort) {
+    using Tr = AttnTraits<FP8, STAGES, TPS>;
     const int lane = threadIdx.x & 31;
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Tr::kOffInfo);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
     uint64_t *empty = full + STAGES;
     const uint64_t policy = policy_evict_first();
-    const uint32_t q_bytes = (uint32_t)(p.G * kHeadDim * Tr::kElem);
-    uint32_t it = 0;
+    ProducerState ps{0u, false, 0u};
     bool ok = true;
 
-    for (int d = d_begin; d < d_end && ok; ++d) {
-        const int4 ds = p.desc[d];
-        const int h = ds.x, r = ds.y, tb = ds.z, te = ds.w;
-        if (tb >= te) continue;  // empty split of the static schedule
-        const int L = p.seqlens[r];
-        float qs = 1.f;
-        if (FP8 && lane < p.G) qs = p.q_scale[(size_t)r * p.Hq + h * p.G + lane];
-        float qsg[kMaxGroup];
-#pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
-        const int32_t *bt_row = p.block_table + (size_t)r * p.max_pages;
-        const uint8_t *q_src = static_cast<const uint8_t *>(p.q) +
-                               ((size_t)r * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
-
-        for (int t0 = tb; t0 < te && ok; t0 += 32) {
-            const int nt = min(32, te - t0);
-            int page = 0;
-            if (lane < nt) {
-                page = bt_row[t0 + lane];
-                if (page < 0 || page >= p.num_pages) {
-                    atomicOr(p.meta + 3, (int)HPC_FLAG_BAD_PAGE);
-                    page = 0;  // stay inside the cache; the result is flagged as invalid
-                }
-            }
-            for (int k = 0; k < nt; ++k) {
-                const int pg = __shfl_sync(kFullMask, page, k);
-                const int stage = it % STAGES;
-                const uint32_t phase = (it / STAGES) & 1u;
-                if (!warp_wait(&empty[stage], phase ^ 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    const int t = t0 + k;
-                    const bool first = t == tb;
-                    StageInfo &si = info[stage];
-                    si.kv_head = h;
-                    si.req = r;
-                    si.tile = t;
-                    si.flags = (first ? kFirst : 0) | (t == te - 1 ? kLast : 0);
-                    si.seqlen = L;
-                    si.desc_idx = d;
-#pragma unroll
-                    for (int g = 0; g < kMaxGroup; ++g) si.qscale[g] = qsg[g];
-                    mbar_arrive_expect_tx(&full[stage],
-                                          2u * Tr::kTileBytes + (first ? q_bytes : 0u));
-                    uint8_t *sk = smem + Tr::kOffK + stage * Tr::kTileBytes;
-                    uint8_t *sv = smem + Tr::kOffV + stage * Tr::kTileBytes;
-                    if (FP8) {
-                        tma_load_4d(sk, tmap_k, &full[stage], 0, h, 0, pg, policy);
-                        tma_load_4d(sv, tmap_v, &full[stage], 0, h, 0, pg, policy);
-                    } else {
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            tma_load_5d(sk + half * Tr::kHalfBytes, tmap_k, &full[stage], 0, half,
-                                        h, 0, pg, policy);
-                            tma_load_5d(sv + half * Tr::kHalfBytes, tmap_v, &full[stage], 0, half,
-                                        h, 0, pg, policy);
-                        }
-                    }
-                    if (first)
-                        bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes, q_src, q_bytes,
-                                  &full[stage]);
-                }
-                __syncwarp();
-                ++it;
-            }
+    // The task map is read only after grid_dependency_wait (the assign kernel
+    // may still be running when this grid starts).  The first descriptor of
+    // the first bin needs no map: it is derived from the sequence lengths
+    // (caller inputs, complete before the assign kernel passed its own wait),
+    // so streaming starts at once.
+    int skip = 0;  // descriptors of the first bin already streamed
+    if (p.fly) {
+        int h, r, tb, te;
+        if (first_descriptor(p, blockIdx.x, h, r, tb, te) && te > tb) {
+            ok = stream_desc<FP8, STAGES, TPS>(tmap_k, tmap_v, p, smem, h, r, tb, te, -1,
+                                               blockIdx.x, ps, policy, abort);
+            skip = 1;
         }
     }
+    wait_for_map(ps);
+
+    // Bins: CTA c starts with bin c; with more bins than CTAs the rest are
+    // pulled in order from a device counter (the grab for the following bin
+    // is issued when a bin starts, so its latency hides behind the stream).
+    const bool dynamic = p.num_bins > (int)gridDim.x;
+    int bin = blockIdx.x;
+    while (ok) {
+        int grab = 0;
+        if (dynamic && lane == 0) grab = atomicAdd(p.bin_counter, 1);
+        const int d_begin = p.bin_ptr[bin] + (bin == (int)blockIdx.x ? skip : 0);
+        const int d_end = p.bin_ptr[bin + 1];
+        for (int d = d_begin; d < d_end && ok; ++d) {
+            const int4 ds = p.desc[d];
+            ok = stream_desc<FP8, STAGES, TPS>(tmap_k, tmap_v, p, smem, ds.x, ds.y, ds.z, ds.w, d,
+                                               bin, ps, policy, abort);
+        }
+        if (!dynamic) break;
+        grab = __shfl_sync(kFullMask, grab, 0);
+        if (grab == p.num_bins - 1 && lane == 0) *p.bin_counter = 0;  // last grab of the launch
+        bin = (int)gridDim.x + grab;
+        if (bin >= p.num_bins) break;
+    }
     if (ok) {  // terminator
-        const int stage = it % STAGES;
-        if (warp_wait(&empty[stage], ((it / STAGES) & 1u) ^ 1u, abort)) {
+        const int stage = ps.it % STAGES;
+        if (warp_wait(&empty[stage], ((ps.it / STAGES) & 1u) ^ 1u, abort)) {
             if (lane == 0) {
                 info[stage].flags = kEnd;
                 mbar_arrive(&full[stage]);
             }
-            ++it;
+            ++ps.it;
         } else {
             ok = false;
         }
     }
-    if (!ok && lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
+    if (!ok) ps.late_flags |= HPC_FLAG_TIMEOUT;
+    const unsigned flags = __reduce_or_sync(kFullMask, ps.late_flags);
+    if (flags && lane == 0) atomicOr(p.meta + 3, (int)flags);
     // Before leaving, make sure no copy this warp issued is still in flight
     // (bounded as well): the last phase issued on every stage must complete.
     if (lane == 0) {
         volatile int no_abort = 0;
-        const uint32_t from = it > (uint32_t)STAGES ? it - STAGES : 0u;
-        for (uint32_t j = from; j < it; ++j)
+        const uint32_t from = ps.it > (uint32_t)STAGES ? ps.it - STAGES : 0u;
+        for (uint32_t j = from; j < ps.it; ++j)
             mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, &no_abort);
     }
     __syncwarp();
 }
 
-// Merge of the four consumer warps' softmax states at the end of a
-// descriptor, then the partial output (normalised, times v_scale) and its
-// natural-log LSE are written to split-buffer slot `desc_idx`.
-template <bool FP8, int STAGES>
-__device__ __forceinline__ bool attn_epilogue(const AttnParams &p, uint8_t *smem,
-                                              const float (&o)[8][4], float m0, float m1,
-                                              float l0, float l1, int desc_idx, uint32_t parity,
-                                              volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES>;
-    constexpr int S = Tr::kCombStride;
-    const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
-    const int g = lane >> 2, t4 = lane & 3;
-    float *comb = reinterpret_cast<float *>(smem + Tr::kOffComb);
-    float *stat_m = reinterpret_cast<float *>(smem + Tr::kOffStat);
-    float *stat_l = stat_m + kConsumerWarps * kMaxGroup;
-    // the four consumer warps meet twice (states written / states consumed)
-    // on an mbarrier pair with bounded waits
-    uint64_t *comb_full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar) + 2 * STAGES;
-    uint64_t *comb_done = comb_full + 1;
-
+// Merge of split unit `di` for query head hd by one warp: lane l owns dims
+// 4l .. 4l + 3; LSEs are read lane-parallel and their weights broadcast by
+// shuffle, with eight partial rows in flight at a time.
+__device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescInfo &di, int hd) {
+    const int lane = threadIdx.x & 31;
+    const float *lse = p.part_lse + (size_t)di.chunk_off * p.G + hd;
+    const float4 *po = reinterpret_cast<const float4 *>(
+                           p.part_o + ((size_t)di.chunk_off * p.G + hd) * kHeadDim) + lane;
+    const size_t row = (size_t)p.G * kHeadDim / 4;  // float4s between chunk rows
+    float4 x[8];
 #pragma unroll
-    for (int o_ = 4; o_ <= 16; o_ <<= 1) {
-        l0 += __shfl_xor_sync(kFullMask, l0, o_);
-        l1 += __shfl_xor_sync(kFullMask, l1, o_);
-    }
-    float *mine = comb + cw * kMaxGroup * S;
-    float *row0 = mine + (2 * t4) * S, *row1 = mine + (2 * t4 + 1) * S;
+    for (int j = 0; j < 8; ++j)
+        x[j] = j < di.count ? __ldcg(po + (size_t)j * row) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float lv0 = lane < di.count ? __ldcg(lse + (size_t)lane * p.G) : kNegInf;
+    float m = lv0;
+    for (int i = 32 + lane; i < di.count; i += 32) m = fmaxf(m, __ldcg(lse + (size_t)i * p.G));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (FP8) {  // m-tile j, row g <-> dim 16g + 2j, row g + 8 <-> 16g + 2j + 1
-            const int dd = 16 * g + 2 * j;
-            *reinterpret_cast<float2 *>(row0 + dd) = make_float2(o[j][0], o[j][2]);
-            *reinterpret_cast<float2 *>(row1 + dd) = make_float2(o[j][1], o[j][3]);
-        } else {  // m-tile j, row g <-> dim 16j + g, row g + 8 <-> 16j + g + 8
-            const int dd = 16 * j + g;
-            row0[dd] = o[j][0];
-            row1[dd] = o[j][1];
-            row0[dd + 8] = o[j][2];
-            row1[dd + 8] = o[j][3];
+    for (int o_ = 16; o_ > 0; o_ >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o_));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    for (int base = 0; base < di.count; base += 32) {
+        const int cnt = min(32, di.count - base);
+        float wl = 0.f;
+        if (lane < cnt)
+            wl = ex2(((base ? __ldcg(lse + (size_t)(base + lane) * p.G) : lv0) - m) * kLog2e);
+        float ws = wl;
+#pragma unroll
+        for (int o_ = 16; o_ > 0; o_ >>= 1) ws += __shfl_xor_sync(kFullMask, ws, o_);
+        wsum += ws;
+        for (int i0 = 0; i0 < cnt; i0 += 8) {
+            if (base | i0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = i0 + j < cnt ? __ldcg(po + (size_t)(base + i0 + j) * row)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = __shfl_sync(kFullMask, wl, (i0 + j) & 31);
+                acc.x += w * x[j].x; acc.y += w * x[j].y;
+                acc.z += w * x[j].z; acc.w += w * x[j].w;
+            }
         }
     }
-    if (g == 0) {
-        stat_m[cw * kMaxGroup + 2 * t4] = m0;
-        stat_m[cw * kMaxGroup + 2 * t4 + 1] = m1;
-        stat_l[cw * kMaxGroup + 2 * t4] = l0;
-        stat_l[cw * kMaxGroup + 2 * t4 + 1] = l1;
-    }
-    mbar_arrive(comb_full);  // every lane releases its own writes
-    if (!warp_wait(comb_full, parity, abort)) return false;
-
-    const int ct = cw * 32 + lane;
-    const int head = ct >> 4, part = ct & 15;
-    if (head < p.G) {
-        float mw[kConsumerWarps], M = kNegInf;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            mw[w] = stat_m[w * kMaxGroup + head];
-            M = fmaxf(M, mw[w]);
-        }
-        const float Ms = M == kNegInf ? 0.f : M;
-        float wsum = 0.f, wt[kConsumerWarps];
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            wt[w] = ex2(mw[w] - Ms);
-            wsum += wt[w] * stat_l[w * kMaxGroup + head];
-        }
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float *src = comb + (w * kMaxGroup + head) * S;
-            const float4 x = *reinterpret_cast<const float4 *>(src + 4 * part);
-            const float4 y = *reinterpret_cast<const float4 *>(src + 64 + 4 * part);
-            a.x += wt[w] * x.x; a.y += wt[w] * x.y; a.z += wt[w] * x.z; a.w += wt[w] * x.w;
-            b.x += wt[w] * y.x; b.y += wt[w] * y.y; b.z += wt[w] * y.z; b.w += wt[w] * y.w;
-        }
-        const float inv = p.v_scale / wsum;
-        float *dst = p.part_o + ((size_t)desc_idx * p.G + head) * kHeadDim;
-        *reinterpret_cast<float4 *>(dst + 4 * part) =
-            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        *reinterpret_cast<float4 *>(dst + 64 + 4 * part) =
-            make_float4(b.x * inv, b.y * inv, b.z * inv, b.w * inv);
-        if (part == 0) p.part_lse[(size_t)desc_idx * p.G + head] = (Ms + lg2(wsum)) * kLn2;
-    }
-    mbar_arrive(comb_done);
-    return warp_wait(comb_done, parity, abort);  // the buffer may be rewritten after this
+    const float inv = 1.f / wsum;
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) +
+                         ((size_t)di.req * p.Hq + di.kv_head * p.G + hd) * kHeadDim + 4 * lane;
+    *reinterpret_cast<uint2 *>(dst) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
-template <bool FP8, int STAGES>
-__device__ __forceinline__ void attn_consumer(const AttnParams &p, uint8_t *smem,
+// ------------------------------------------------------------------ combiner
+// Register r = 4 j + e of accumulator lane (g, t4) holds (dim, head):
+//   head = 2 t4 + (e & 1);
+//   BF16: dim = 16 j + g + 8 (e >> 1)   (m-tile j, rows g and g + 8)
+//   FP8:  dim = 16 g + 2 j + (e >> 1)   (permuted rows, see the consumer)
+template <bool FP8>
+__device__ __forceinline__ int state_dim(int r, int g) {
+    const int j = r >> 2, e = r & 3;
+    return FP8 ? 16 * g + 2 * j + (e >> 1) : 16 * j + g + 8 * (e >> 1);
+}
+
+// Column of `dim` in a staging row: the float4 group is XOR-ed with
+// (dim / 16) % 8, which spreads the combiner's scalar writes over more
+// banks (FP8 lanes own 16 consecutive dims) while keeping float4 reads of
+// dims 4q .. 4q + 3 contiguous.
+__device__ __forceinline__ int stage_col(int dim) { return dim ^ (((dim >> 4) & 7) << 2); }
+
+// Merges the consumers' states of each finished descriptor and writes the
+// result; counts chunks of split units.  Returns false after a timeout.
+template <bool FP8, int STAGES, int TPS>
+__device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem,
                                               volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES>;
-    const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
+    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    constexpr int NC = Tr::kConsumers;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    const float *comb = reinterpret_cast<const float *>(smem + Tr::kOffComb);
+    float *stage = reinterpret_cast<float *>(smem + Tr::kOffStage);
+    const SlotInfo *slots = reinterpret_cast<const SlotInfo *>(smem + Tr::kOffSlotInfo);
+    SlotInfo *last = reinterpret_cast<SlotInfo *>(smem + Tr::kOffLast);  // [0].flags = count
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
+    uint64_t *slot_full = bars + 2 * STAGES, *slot_empty = slot_full + kCombSlots;
+    const bool fused = p.out != nullptr;
+    int nlast = 0;
+
+    for (uint32_t n = 0;; ++n) {
+        const int k = n % kCombSlots;
+        if (!warp_wait(&slot_full[k], (n / kCombSlots) & 1u, abort)) return false;
+        const SlotInfo si = slots[k];
+        if (si.flags & kEnd) break;
+        // [warp][lane][36]: this lane's 9 float4 of every consumer warp
+        const float4 *st = reinterpret_cast<const float4 *>(comb + k * Tr::kSlotFloats) + lane * 9;
+        float4 ml[NC];
+        float M0 = kNegInf, M1 = kNegInf;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+            ml[w] = st[w * 32 * 9 + 8];  // (m0, m1, l0, l1)
+            M0 = fmaxf(M0, ml[w].x);
+            M1 = fmaxf(M1, ml[w].y);
+        }
+        const float Z0 = M0 == kNegInf ? 0.f : M0, Z1 = M1 == kNegInf ? 0.f : M1;
+        float acc[32], L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) acc[r] = 0.f;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+            const float a0 = ex2(ml[w].x - Z0), a1 = ex2(ml[w].y - Z1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = st[w * 32 * 9 + j];
+                acc[4 * j + 0] += v.x * a0;
+                acc[4 * j + 1] += v.y * a1;
+                acc[4 * j + 2] += v.z * a0;
+                acc[4 * j + 3] += v.w * a1;
+            }
+            L0 += ml[w].z * a0;
+            L1 += ml[w].w * a1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&slot_empty[k]);  // the consumers may refill the slot
+#pragma unroll
+        for (int o_ = 4; o_ <= 16; o_ <<= 1) {  // per-head sums over the tokens of all lanes
+            L0 += __shfl_xor_sync(kFullMask, L0, o_);
+            L1 += __shfl_xor_sync(kFullMask, L1, o_);
+        }
+        const float inv0 = p.v_scale / L0, inv1 = p.v_scale / L1;
+        // stage the normalised result as [head][dim] for coalesced stores
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            stage[(2 * t4 + (r & 1)) * kStageStride + stage_col(state_dim<FP8>(r, g))] =
+                acc[r] * ((r & 1) ? inv1 : inv0);
+        __syncwarp();
+        const DescInfo di = si.di;
+        const bool direct = fused && di.count == 1;
+        if (direct) {  // the unit's only chunk: final BF16 output
+            for (int h = 0; h < p.G; ++h) {
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(stage + h * kStageStride + stage_col(4 * lane));
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) +
+                                     ((size_t)di.req * p.Hq + di.kv_head * p.G + h) * kHeadDim;
+                reinterpret_cast<uint2 *>(dst)[lane] =
+                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            }
+        } else {  // partial + LSE, kept in L2 for the CTA (or kernel) that merges
+            const uint64_t keep = policy_evict_last();
+            for (int h = 0; h < p.G; ++h) {
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(stage + h * kStageStride + stage_col(4 * lane));
+                float *dst = p.part_o + ((size_t)di.desc_idx * p.G + h) * kHeadDim;
+                st_global_hint(reinterpret_cast<float4 *>(dst) + lane, v, keep);
+            }
+            if (g == 0) {
+                const float lse0 = (Z0 + lg2(L0)) * kLn2, lse1 = (Z1 + lg2(L1)) * kLn2;
+                float *dl = p.part_lse + (size_t)di.desc_idx * p.G;
+                if (2 * t4 < p.G) st_global_hint(dl + 2 * t4, lse0, keep);
+                if (2 * t4 + 1 < p.G) st_global_hint(dl + 2 * t4 + 1, lse1, keep);
+            }
+            if (fused) {  // count this chunk of a split unit
+                __syncwarp();  // every lane's partial stores precede lane 0's release below
+                int completes = 0;
+                if (lane == 0) {
+                    int *ctr = p.unit_done + di.kv_head * p.B + di.req;
+                    const int prev = atom_add_acq_rel_gpu(ctr, 1);
+                    if (prev == di.count - 1) {  // this CTA completes the unit
+                        *ctr = 0;                 // every chunk counted: ready for the next launch
+                        completes = 1;
+                    }
+                }
+                if (__shfl_sync(kFullMask, completes, 0)) {
+                    if (nlast < kMaxLast) {  // merged at the end by all warps
+                        if (lane == 0) last[1 + nlast].di = di;
+                        ++nlast;
+                    } else {  // list full (many bins per CTA): merge here, alone
+                        for (int h = 0; h < p.G; ++h) merge_unit_head(p, di, h);
+                    }
+                }
+            }
+        }
+        __syncwarp();  // the staging area is rewritten by the next descriptor
+    }
+    if (lane == 0) last[0].flags = nlast;
+    return true;
+}
+
+// ------------------------------------------------------------------ consumer
+template <bool FP8, int STAGES, int TPS>
+__device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem,
+                                              volatile int *abort) {
+    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 2;
     const int g = lane >> 2, t4 = lane & 3;
+    const int slot = cw >> 2;  // which tile of the stage this warp works on
+    const int sub = cw & 3;    // which 16 tokens of that tile
     const StageInfo *info = reinterpret_cast<const StageInfo *>(smem + Tr::kOffInfo);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
     uint64_t *empty = full + STAGES;
-    const uint32_t sK0 = smem_u32(smem + Tr::kOffK), sV0 = smem_u32(smem + Tr::kOffV);
+    uint64_t *slot_full = full + 2 * STAGES, *slot_empty = slot_full + kCombSlots;
+    float *comb = reinterpret_cast<float *>(smem + Tr::kOffComb);
+    SlotInfo *slots = reinterpret_cast<SlotInfo *>(smem + Tr::kOffSlotInfo);
+    const uint32_t sK0 = smem_u32(smem + Tr::kOffK) + slot * Tr::kTileBytes;
+    const uint32_t sV0 = smem_u32(smem + Tr::kOffV) + slot * Tr::kTileBytes;
 
     // Lane-constant parts of the shared-memory addresses.  ldmatrix: lane
     // supplies row (lane & 7) of matrix (lane >> 3).
     const int mi = lane >> 3;
-    const int tok_k = 16 * cw + (lane & 7) + (mi & 1) * 8;  // K: matrices 1, 3 = rows 8..15
-    const int tok_v = 16 * cw + (lane & 7) + (mi >> 1) * 8;  // V^T: matrices 2, 3 = toks 8..15
+    const int tok_k = 16 * sub + (lane & 7) + (mi & 1) * 8;  // K: matrices 1, 3 = rows 8..15
+    const int tok_v = 16 * sub + (lane & 7) + (mi >> 1) * 8;  // V^T: matrices 2, 3 = toks 8..15
 
     float o[8][4];
     float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f, sc0 = 0.f, sc1 = 0.f;
@@ -295,171 +578,200 @@ __device__ __forceinline__ void attn_consumer(const AttnParams &p, uint8_t *smem
         qf[j][0] = qf[j][1] = 0u;
     }
 
-    uint32_t epilogues = 0;
+    uint32_t handed = 0;  // descriptors handed to the combiner
     for (uint32_t it = 0;; ++it) {
         const int stage = it % STAGES;
-        if (!warp_wait(&full[stage], (it / STAGES) & 1u, abort)) {
-            if (lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
-            break;
-        }
+        if (!warp_wait(&full[stage], (it / STAGES) & 1u, abort)) return false;
         const int flags = info[stage].flags;
-        if (flags & kEnd) break;
-        const int tile = info[stage].tile, L = info[stage].seqlen;
-        const int desc_idx = info[stage].desc_idx;
-        const uint32_t sK = sK0 + stage * Tr::kTileBytes, sV = sV0 + stage * Tr::kTileBytes;
+        const int ntiles = info[stage].ntiles, tile0 = info[stage].tile0;
+        const int L = info[stage].seqlen;
+        DescInfo di;
+        if (flags & kLast)
+            di = {info[stage].req, info[stage].kv_head, info[stage].desc_idx, info[stage].count,
+                  info[stage].chunk_off};
 
-        if (flags & kFirst) {  // new descriptor: load Q^T fragments, reset the state
-            // B fragment of Q^T (k = dim, n = head): lane holds head g, dims
-            // 2t4.. (bf16) or 4t4.. (e4m3) of each k-step, and +8 / +16 beyond.
-            const uint8_t *q = smem + Tr::kOffQ + stage * Tr::kQBytes + g * kHeadDim * Tr::kElem;
-            const bool live = g < p.G;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                if (FP8 && s >= 4) break;
-                const int off = FP8 ? 32 * s + 4 * t4 : 2 * (16 * s + 2 * t4);
-                qf[s][0] = live ? *reinterpret_cast<const uint32_t *>(q + off) : 0u;
-                qf[s][1] = live ? *reinterpret_cast<const uint32_t *>(q + off + 16) : 0u;
+        if (!(flags & kEnd)) {
+            if (flags & kFirst) {  // new descriptor: load Q^T fragments, reset the state
+                // B fragment of Q^T (k = dim, n = head): lane holds head g, dims
+                // 2t4.. (bf16) or 4t4.. (e4m3) of each k-step, and +8 / +16 beyond.
+                const uint8_t *q = smem + Tr::kOffQ + stage * Tr::kQBytes + g * kHeadDim * Tr::kElem;
+                const bool live = g < p.G;
+    #pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    if (FP8 && s >= 4) break;
+                    const int off = FP8 ? 32 * s + 4 * t4 : 2 * (16 * s + 2 * t4);
+                    qf[s][0] = live ? *reinterpret_cast<const uint32_t *>(q + off) : 0u;
+                    qf[s][1] = live ? *reinterpret_cast<const uint32_t *>(q + off + 16) : 0u;
+                }
+                sc0 = p.score_scale * info[stage].qscale[2 * t4];
+                sc1 = p.score_scale * info[stage].qscale[2 * t4 + 1];
+                m0 = m1 = kNegInf;
+                l0 = l1 = 0.f;
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             }
-            sc0 = p.score_scale * info[stage].qscale[2 * t4];
-            sc1 = p.score_scale * info[stage].qscale[2 * t4 + 1];
-            m0 = m1 = kNegInf;
-            l0 = l1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        }
 
-        // ---- S^T = K . Q^T for this warp's 16 tokens x 8 heads
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-        if (FP8) {
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int chunk = 2 * s + (mi >> 1);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(sK + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4), a0, a1, a2, a3);
-                mma_e4m3_16832(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-            }
-        } else {
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int chunk = (2 * s + (mi >> 1)) & 7;
-                const uint32_t addr =
-                    sK + (s >> 2) * Tr::kHalfBytes + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(addr, a0, a1, a2, a3);
-                mma_bf16_16816(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-            }
-        }
+            if (slot < ntiles) {
+                const uint32_t sK = sK0 + stage * Tr::kStageKV, sV = sV0 + stage * Tr::kStageKV;
+                const int tile = tile0 + slot;
 
-        // ---- online softmax (log2 domain); tokens at or past L are masked
-        const int tok0 = tile * kTile + 16 * cw;  // first token of this warp's slice
-        const bool va = tok0 + g < L, vb = tok0 + g + 8 < L;
-        const float x0 = va ? s4[0] * sc0 : kNegInf, x1 = va ? s4[1] * sc1 : kNegInf;
-        const float x2 = vb ? s4[2] * sc0 : kNegInf, x3 = vb ? s4[3] * sc1 : kNegInf;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int o_ = 4; o_ <= 16; o_ <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, o_));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, o_));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == kNegInf ? 0.f : mn0, ms1 = mn1 == kNegInf ? 0.f : mn1;
-        const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
-        m0 = mn0;
-        m1 = mn1;
-        const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-        const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-        uint32_t pk01, pk23;
-        if (FP8) {
-            pk01 = pack_f16x2(p0, p1);
-            pk23 = pack_f16x2(p2, p3);
-            const float2 r01 = f16x2_to_f32x2(pk01), r23 = f16x2_to_f32x2(pk23);
-            l0 = l0 * al0 + r01.x + r23.x;
-            l1 = l1 * al1 + r01.y + r23.y;
-        } else {
-            pk01 = pack_bf16x2(p0, p1);
-            pk23 = pack_bf16x2(p2, p3);
-            l0 = l0 * al0 + bf16lo_to_f32(pk01) + bf16lo_to_f32(pk23);
-            l1 = l1 * al1 + bf16hi_to_f32(pk01) + bf16hi_to_f32(pk23);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            o[j][0] *= al0;
-            o[j][1] *= al1;
-            o[j][2] *= al0;
-            o[j][3] *= al1;
-        }
-        // P^T fragments (k = token, n = head): transpose the 8x8 halves
-        const uint32_t b0 = movmatrix_trans(pk01), b1 = movmatrix_trans(pk23);
+                // ---- S^T = K . Q^T for this warp's 16 tokens x 8 heads
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (FP8) {
+    #pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const int chunk = 2 * s + (mi >> 1);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(sK + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4), a0, a1, a2, a3);
+                        mma_e4m3_16832(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                    }
+                } else {
+                    float s4b[4] = {0.f, 0.f, 0.f, 0.f};  // two chains: even / odd k-steps
+    #pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const int chunk = (2 * s + (mi >> 1)) & 7;
+                        const uint32_t addr = sK + (s >> 2) * Tr::kHalfBytes + tok_k * 128 +
+                                              ((chunk ^ (tok_k & 7)) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(addr, a0, a1, a2, a3);
+                        if (s & 1)
+                            mma_bf16_16816(s4b, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                        else
+                            mma_bf16_16816(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                    }
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) s4[e] += s4b[e];
+                }
 
-        // ---- O^T += V^T . P^T
-        if (FP8) {
-            // rows 2t4, 2t4+1, 2t4+8, 2t4+9 of the slice; dims 16g .. 16g+15
-            uint4 R[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tok = 16 * cw + 2 * t4 + (q & 1) + (q >> 1) * 8;
-                R[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
-                if (tile * kTile + tok >= L) R[q] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            const uint32_t wA[4] = {R[0].x, R[0].y, R[0].z, R[0].w};
-            const uint32_t wB[4] = {R[1].x, R[1].y, R[1].z, R[1].w};
-            const uint32_t wC[4] = {R[2].x, R[2].y, R[2].z, R[2].w};
-            const uint32_t wD[4] = {R[3].x, R[3].y, R[3].z, R[3].w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
-                const uint32_t x01 = __byte_perm(wA[j >> 1], wB[j >> 1], sel);
-                const uint32_t x23 = __byte_perm(wC[j >> 1], wD[j >> 1], sel);
-                uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(x01, a0, a1);
-                e4m3x4_to_f16x2x2(x23, a2, a3);
-                mma_f16_16816(o[j], a0, a1, a2, a3, b0, b1);
-            }
-        } else {
-            const int tv = tok0 + 2 * t4;  // tokens of a0/a1 halves; +8 for a2/a3
-            const uint32_t mk01 = (tv < L ? 0x0000ffffu : 0u) | (tv + 1 < L ? 0xffff0000u : 0u);
-            const uint32_t mk23 =
-                (tv + 8 < L ? 0x0000ffffu : 0u) | (tv + 9 < L ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int chunk = (2 * j + (mi & 1)) & 7;
-                const uint32_t addr =
-                    sV + (j >> 2) * Tr::kHalfBytes + tok_v * 128 + ((chunk ^ (tok_v & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(addr, a0, a1, a2, a3);
-                mma_bf16_16816(o[j], a0 & mk01, a1 & mk01, a2 & mk23, a3 & mk23, b0, b1);
+                // ---- online softmax (log2 domain); tokens at or past L are masked
+                const int tok0 = tile * kTile + 16 * sub;  // first token of this warp's slice
+                const bool va = tok0 + g < L, vb = tok0 + g + 8 < L;
+                const float x0 = va ? s4[0] * sc0 : kNegInf, x1 = va ? s4[1] * sc1 : kNegInf;
+                const float x2 = vb ? s4[2] * sc0 : kNegInf, x3 = vb ? s4[3] * sc1 : kNegInf;
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    #pragma unroll
+                for (int o_ = 4; o_ <= 16; o_ <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, o_));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, o_));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float ms0 = mn0 == kNegInf ? 0.f : mn0, ms1 = mn1 == kNegInf ? 0.f : mn1;
+                const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
+                m0 = mn0;
+                m1 = mn1;
+                const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
+                const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
+                uint32_t pk01, pk23;
+                if (FP8) {
+                    pk01 = pack_f16x2(p0, p1);
+                    pk23 = pack_f16x2(p2, p3);
+                    const float2 r01 = f16x2_to_f32x2(pk01), r23 = f16x2_to_f32x2(pk23);
+                    l0 = l0 * al0 + r01.x + r23.x;
+                    l1 = l1 * al1 + r01.y + r23.y;
+                } else {
+                    pk01 = pack_bf16x2(p0, p1);
+                    pk23 = pack_bf16x2(p2, p3);
+                    l0 = l0 * al0 + bf16lo_to_f32(pk01) + bf16lo_to_f32(pk23);
+                    l1 = l1 * al1 + bf16hi_to_f32(pk01) + bf16hi_to_f32(pk23);
+                }
+                if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {  // rescale only on a new max
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        o[j][0] *= al0;
+                        o[j][1] *= al1;
+                        o[j][2] *= al0;
+                        o[j][3] *= al1;
+                    }
+                }
+                // P^T fragments (k = token, n = head): transpose the 8x8 halves
+                const uint32_t b0 = movmatrix_trans(pk01), b1 = movmatrix_trans(pk23);
+
+                // ---- O^T += V^T . P^T
+                if (FP8) {
+                    // rows 2t4, 2t4+1, 2t4+8, 2t4+9 of the slice; dims 16g .. 16g+15
+                    uint4 R[4];
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 16 * sub + 2 * t4 + (q & 1) + (q >> 1) * 8;
+                        R[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
+                        if (tile * kTile + tok >= L) R[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    const uint32_t wA[4] = {R[0].x, R[0].y, R[0].z, R[0].w};
+                    const uint32_t wB[4] = {R[1].x, R[1].y, R[1].z, R[1].w};
+                    const uint32_t wC[4] = {R[2].x, R[2].y, R[2].z, R[2].w};
+                    const uint32_t wD[4] = {R[3].x, R[3].y, R[3].z, R[3].w};
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
+                        const uint32_t x01 = __byte_perm(wA[j >> 1], wB[j >> 1], sel);
+                        const uint32_t x23 = __byte_perm(wC[j >> 1], wD[j >> 1], sel);
+                        uint32_t a0, a1, a2, a3;
+                        e4m3x4_to_f16x2x2(x01, a0, a1);
+                        e4m3x4_to_f16x2x2(x23, a2, a3);
+                        mma_f16_16816(o[j], a0, a1, a2, a3, b0, b1);
+                    }
+                } else {
+                    const int tv = tok0 + 2 * t4;  // tokens of a0/a1 halves; +8 for a2/a3
+                    const uint32_t mk01 =
+                        (tv < L ? 0x0000ffffu : 0u) | (tv + 1 < L ? 0xffff0000u : 0u);
+                    const uint32_t mk23 =
+                        (tv + 8 < L ? 0x0000ffffu : 0u) | (tv + 9 < L ? 0xffff0000u : 0u);
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int chunk = (2 * j + (mi & 1)) & 7;
+                        const uint32_t addr = sV + (j >> 2) * Tr::kHalfBytes + tok_v * 128 +
+                                              ((chunk ^ (tok_v & 7)) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(addr, a0, a1, a2, a3);
+                        mma_bf16_16816(o[j], a0 & mk01, a1 & mk01, a2 & mk23, a3 & mk23, b0, b1);
+                    }
+                }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);  // stage may now be refilled
+        if (lane == 0 && !(flags & kEnd)) mbar_arrive(&empty[stage]);  // stage may be refilled
 
-        if (flags & kLast) {
-            if (!attn_epilogue<FP8, STAGES>(p, smem, o, m0, m1, l0, l1, desc_idx,
-                                            epilogues & 1u, abort)) {
-                if (lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
-                break;
+        if (flags & (kLast | kEnd)) {  // hand the state (or the end) to the combiner
+            const int k = handed % kCombSlots;
+            if (!warp_wait(&slot_empty[k], ((handed / kCombSlots) & 1u) ^ 1u, abort))
+                return false;
+            if (flags & kLast) {  // lane-major: 9 float4 per lane, conflict-free
+                float4 *dst = reinterpret_cast<float4 *>(
+                    comb + ((k * Tr::kConsumers + cw) * 32 + lane) * kStateRegs);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
+                dst[8] = make_float4(m0, m1, l0, l1);
+                if (cw == 0 && lane == 0) slots[k] = SlotInfo{di, 0, 0, 0};
+            } else if (cw == 0 && lane == 0) {
+                slots[k].flags = kEnd;
             }
-            ++epilogues;
+            mbar_arrive(&slot_full[k]);  // every lane releases its own writes
+            ++handed;
+            if (flags & kEnd) return true;
         }
     }
 }
 
-template <bool FP8, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// ------------------------------------------------------------------ kernel
+template <bool FP8, int STAGES, int TPS>
+__global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
-    using Tr = AttnTraits<FP8, STAGES>;
+    using Tr = AttnTraits<FP8, STAGES, TPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + Tr::kOffAbort);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + Tr::kOffMisc);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);                        // producer arrive + TMA bytes
-            mbar_init(&full[STAGES + s], kConsumerWarps);  // one arrive per consumer warp
+            mbar_init(&bars[s], 1);                          // full: producer arrive + TMA bytes
+            mbar_init(&bars[STAGES + s], Tr::kConsumers);    // empty: one arrive per consumer warp
         }
-        mbar_init(&full[2 * STAGES], 32 * kConsumerWarps);      // epilogue: states written
-        mbar_init(&full[2 * STAGES + 1], 32 * kConsumerWarps);  // epilogue: states consumed
+        for (int k = 0; k < kCombSlots; ++k) {
+            mbar_init(&bars[2 * STAGES + k], 32 * Tr::kConsumers);   // slot full: every consumer lane
+            mbar_init(&bars[2 * STAGES + kCombSlots + k], 1);        // slot empty: the combiner
+        }
+        mbar_init(&bars[2 * STAGES + 2 * kCombSlots], 32 * (Tr::kConsumers + 1));  // end rendezvous
         *abort = 0;
         fence_barrier_init();
     }
@@ -467,12 +779,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
+    // The block table and Q are caller inputs, not outputs of the assign
+    // kernel: warm L2 with this CTA's share of them while the assign kernel
+    // may still be running.
+    {
+        const size_t bt_bytes = (size_t)p.B * p.max_pages * 4;
+        const size_t q_bytes = (size_t)p.B * p.Hq * kHeadDim * Tr::kElem;
+        const char *bt = reinterpret_cast<const char *>(p.block_table);
+        const char *q = static_cast<const char *>(p.q);
+        for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 128; off < bt_bytes;
+             off += (size_t)gridDim.x * blockDim.x * 128)
+            prefetch_l2(bt + off);
+        for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 128; off < q_bytes;
+             off += (size_t)gridDim.x * blockDim.x * 128)
+            prefetch_l2(q + off);
+    }
+    // No grid-wide wait here: only the producer reads the task map, and it
+    // waits for the assign kernel right before it first needs the map.
+    grid_launch_dependents();
     __syncthreads();
-    const int d_begin = p.bin_ptr[blockIdx.x], d_end = p.bin_ptr[blockIdx.x + 1];
-    if (threadIdx.x < 32)
-        attn_producer<FP8, STAGES>(&tmap_k, &tmap_v, p, smem, d_begin, d_end, abort);
-    else
-        attn_consumer<FP8, STAGES>(p, smem, abort);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        attn_producer<FP8, STAGES, TPS>(&tmap_k, &tmap_v, p, smem, abort);
+        return;
+    }
+    // Every global write of this grid (outputs, partials, counters) comes
+    // after the previous grid in the stream has finished: the combiner, idle
+    // until the first hand-off, waits here; the end phase waits below.
+    if (warp == 1) grid_dependency_wait();
+    if (warp == 1 && p.out) {  // fused mode: requests without live tokens get zero rows
+        const int row_vec = p.Hq * kHeadDim * 2 / 16;  // 16-byte vectors per request
+        for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
+            if (p.seqlens[r] > 0) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                   (size_t)r * p.Hq * kHeadDim);
+            for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    bool ok = warp == 1 ? attn_combiner<FP8, STAGES, TPS>(p, smem, abort)
+                        : attn_consumer<FP8, STAGES, TPS>(p, smem, abort);
+    if (!ok) {
+        grid_dependency_wait();  // meta[3] is written by the assign kernel
+        if (lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
+        *abort = 1;
+    }
+    // End of the stream: the combiner has published the split units whose
+    // merge this CTA owes; all non-producer warps merge them, one warp per
+    // (unit, head).
+    uint64_t *end_bar = bars + 2 * STAGES + 2 * kCombSlots;
+    mbar_arrive(end_bar);
+    if (!warp_wait(end_bar, 0, abort)) {
+        grid_dependency_wait();
+        if (lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
+        return;
+    }
+    if (!p.out || *abort) return;
+    grid_dependency_wait();  // (long complete by now) before this warp's first global writes
+    const SlotInfo *last = reinterpret_cast<const SlotInfo *>(smem + Tr::kOffLast);
+    const int nlast = last[0].flags;
+    const int nw = 1 + Tr::kConsumers, w = warp - 1;
+    for (int item = w; item < nlast * p.G; item += nw)
+        merge_unit_head(p, last[1 + item / p.G].di, item % p.G);
 }
 
 }  // namespace hpc

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                    const int32_t *__restrict__ chunk_count, const int32_t *__restrict__ chunk_off,
                    int B, int Hq, int G, __nv_bfloat16 *__restrict__ out) {
+    grid_dependency_wait();  // partials of the attention grid are complete
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);  // r * Hq + hq
     if (row >= B * Hq) return;
@@ -31,6 +32,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     const int n = chunk_count[u];
     const int off = chunk_off[u];
 
+    // LSEs are read lane-parallel (lane i holds chunk base + i) and their
+    // weights broadcast by shuffle, so the partial-row loads of up to four
+    // chunks are in flight together instead of one dependent load per chunk.
     float m = -INFINITY;
     for (int i = lane; i < n; i += 32) m = fmaxf(m, part_lse[(size_t)(off + i) * G + g]);
 #pragma unroll
@@ -38,15 +42,32 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    for (int i = 0; i < n; ++i) {
-        const size_t slot = (size_t)(off + i) * G + g;
-        const float w = ex2((part_lse[slot] - m) * kLog2e);
-        const float4 o = reinterpret_cast<const float4 *>(part_o + slot * kHeadDim)[lane];
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
-        wsum += w;
+    for (int base = 0; base < n; base += 32) {
+        const int cnt = min(32, n - base);
+        const float wl =
+            lane < cnt ? ex2((part_lse[(size_t)(off + base + lane) * G + g] - m) * kLog2e) : 0.f;
+        float ws = wl;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        wsum += ws;
+        for (int k = 0; k < cnt; k += 4) {
+            float4 x[4];
+            float w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[j] = __shfl_sync(0xffffffffu, wl, (k + j) & 31);
+                const size_t slot = (size_t)(off + base + k + j) * G + g;
+                x[j] = k + j < cnt ? reinterpret_cast<const float4 *>(part_o + slot * kHeadDim)[lane]
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc.x += w[j] * x[j].x;
+                acc.y += w[j] * x[j].y;
+                acc.z += w[j] * x[j].z;
+                acc.w += w[j] * x[j].w;
+            }
+        }
     }
     const float inv = n > 0 ? 1.f / wsum : 0.f;
     uint2 packed;
@@ -62,10 +83,19 @@ cudaError_t launch_combine(const float *part_o, const float *part_lse, const hpc
     const int rows = B * Hq;
     if (rows == 0) return cudaSuccess;
     const int grid = (rows + kCombineWarps - 1) / kCombineWarps;
-    combine_kernel<<<grid, 32 * kCombineWarps, 0, s>>>(part_o, part_lse, map.chunk_count,
-                                                       map.chunk_off, B, Hq, Hq / Hkv,
-                                                       static_cast<__nv_bfloat16 *>(out));
-    return cudaGetLastError();
+    // a programmatic dependent of the attention grid: launches during its tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * kCombineWarps);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, part_o, part_lse,
+                              (const int32_t *)map.chunk_count, (const int32_t *)map.chunk_off, B,
+                              Hq, Hq / Hkv, static_cast<__nv_bfloat16 *>(out));
 }
 
 }  // namespace hpc

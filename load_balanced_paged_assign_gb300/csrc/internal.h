@@ -14,8 +14,7 @@ namespace hpc {
 constexpr int kHeadDim = 128;
 constexpr int kTile = 64;  // tokens per tile = tokens per page
 constexpr int kMaxGroup = 8;
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);  // one producer warp + consumers
+constexpr int kConsumerWarps = 4;  // consumer warps per tile of a stage
 constexpr int kPlanThreads = 1024;
 
 // Stage flags written by the producer for the consumers.
@@ -26,6 +25,8 @@ constexpr int kEnd = 4;    // terminator: the bin is drained
 struct AttnParams {
     const int32_t *bin_ptr;
     const int4 *desc;
+    const int32_t *chunk_count;
+    const int32_t *chunk_off;
     const int32_t *seqlens;
     const int32_t *block_table;
     const void *q;
@@ -33,6 +34,12 @@ struct AttnParams {
     float *part_o;
     float *part_lse;
     int32_t *meta;
+    int32_t *unit_done;  // fused mode: per-unit chunk counters (zero between launches)
+    void *out;           // fused mode: BF16 output; nullptr = write partials only
+    int *bin_counter;  // dynamic bins: next bin to pull, minus the grid size
+    int num_bins;      // bins in the task map (>= the grid size)
+    int min_tiles;     // floor the map was planned with (load-balanced maps)
+    int fly;           // 1: derive the first descriptor from the seqlens (load-balanced maps)
     int B, Hq, Hkv, G, max_pages, num_pages;
     float score_scale;  // sm_scale * log2(e), times k_scale for FP8
     float v_scale;      // 1 for BF16
@@ -42,7 +49,7 @@ struct AttnParams {
 struct AttnConfig {
     const void *kernel;
     int smem_bytes;
-    int stages;
+    int threads;
 };
 
 AttnConfig attn_config_bf16();

@@ -85,12 +85,12 @@ extern "C" hpc_status hpc_decode_step_noalloc(
     map.cap_desc = (int32_t)cap;
     map.cap_bins = num_ctas + 1;
     map.cap_units = (int32_t)units;
-    map.B = map.Hkv = map.num_ctas = 0;
+    map.B = map.Hkv = map.num_ctas = map.persistent = map.min_tiles = map.max_pages = 0;
     hpc_status st = hpc_decode_step(
         d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale, kv_dtype,
         d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv, head_dim, sm_scale, num_ctas,
         min_tiles_per_cta, 0, &map, reinterpret_cast<float *>(s + off_part_o),
-        reinterpret_cast<float *>(s + off_part_lse), d_out, stream);
+        reinterpret_cast<float *>(s + off_part_lse), nullptr, d_out, stream);
     if (st != HPC_OK || !d_meta_out) return st;
     return cudaMemcpyAsync(d_meta_out, map.meta, 4 * sizeof(int32_t), cudaMemcpyDeviceToDevice,
                            static_cast<cudaStream_t>(stream)) == cudaSuccess

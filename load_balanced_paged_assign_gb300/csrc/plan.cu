@@ -13,6 +13,7 @@
 // found by locating the unit that owns the bin's first tile.
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace hpc {
 namespace {
@@ -69,6 +70,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     __shared__ int s_scan[32];
     __shared__ unsigned s_flags;
     const int tid = threadIdx.x;
+    grid_dependency_wait();    // launched as a dependent: the previous grid is done
+    grid_launch_dependents();  // the attention grid may start its prologue now
     if (tid == 0) s_flags = 0;
     unsigned flags = 0;
 
@@ -83,15 +86,15 @@ __global__ void __launch_bounds__(kPlanThreads)
         carry += chunk_total;
     }
     __syncthreads();  // s_end complete
-    const int N = carry;  // tiles per KV head; host guarantees Hkv * N < 2^31
+    const int N = carry;  // tiles per KV head; the host keeps Hkv * N < 2^30
     const int T = Hkv * N;
 
     // a2: budget = max(ceil(T / C), floor, 1).
-    int budget = (T + num_ctas - 1) / num_ctas;
-    budget = max(budget, max(floor, 1));
+    const int budget = max((T + num_ctas - 1) / num_ctas, max(floor, 1));
 
-    // a3: chunk counts per unit (head-major, batch-minor), their offsets, and
-    // the descriptors themselves.
+    // a3: chunk counts per unit (head-major, batch-minor), their offsets, the
+    // descriptors, and the CSR offset of every used bin: bin b starts with
+    // the descriptor that holds global tile b * budget.
     const int units = Hkv * B;
     carry = 0;
     for (int base = 0; base < units; base += blockDim.x) {
@@ -113,48 +116,34 @@ __global__ void __launch_bounds__(kPlanThreads)
             const int first_bin = S / budget;
             for (int i = 0; i < cnt; ++i) {
                 const long long bin = first_bin + i;
-                const int lo = (int)max((long long)S, bin * budget);
-                const int hi = (int)min((long long)(S + n), (bin + 1) * budget);
-                if (off + i < cap_desc)
+                const long long bin_lo = bin * budget;
+                const int lo = (int)max((long long)S, bin_lo);
+                const int hi = (int)min((long long)(S + n), bin_lo + budget);
+                if (off + i < cap_desc) {
                     desc[off + i] = make_int4(h, r, lo - S, hi - S);
-                else
+                    if (lo == bin_lo) bin_ptr[bin] = off + i;  // first descriptor of its bin
+                } else {
                     flags |= HPC_FLAG_DESC_OVERFLOW;
+                }
             }
         }
         carry += chunk_total;
     }
     const int num_desc = carry;
     if (flags) atomicOr(&s_flags, flags);
-    __syncthreads();  // chunk_off (global) and s_flags now visible block-wide
+    __syncthreads();
     const bool overflow = (s_flags & HPC_FLAG_DESC_OVERFLOW) != 0;
-
-    // Bin offsets: bin b starts at global tile b * budget.  The unit owning
-    // that tile is found by binary search; its descriptor in bin b has index
-    // chunk_off[u] + (b - first_bin(u)).  Bins past the last tile are empty.
-    for (int b = tid; b <= num_ctas; b += blockDim.x) {
-        int ptr = num_desc;
-        const long long t = (long long)b * budget;
-        if (!overflow && b < num_ctas && t < T) {
-            const int h = (int)(t / N);
-            const int tl = (int)(t - (long long)h * N);
-            int lo = 0, hi = B - 1;  // first r with s_end[r] > tl
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (s_end[mid] > tl) hi = mid; else lo = mid + 1;
-            }
-            const int r = lo;
-            const int n = s_end[r] - (r ? s_end[r - 1] : 0);
-            const int S = h * N + s_end[r] - n;
-            ptr = chunk_off[h * B + r] + (b - S / budget);
-        }
-        if (overflow) ptr = 0;  // an overflowing map is emptied, never half-used
-        bin_ptr[b] = ptr;
-    }
+    // bins past the last tile are empty; an overflowing map is emptied entirely
+    const int used = overflow ? 0 : (T + budget - 1) / budget;
+    for (int b = used + tid; b <= num_ctas; b += blockDim.x) bin_ptr[b] = overflow ? 0 : num_desc;
+    if (overflow)
+        for (int b = tid; b < num_ctas; b += blockDim.x) bin_ptr[b] = 0;
     if (tid == 0) {
         meta[0] = T;
         meta[1] = budget;
         meta[2] = overflow ? 0 : num_desc;
         meta[3] = (int)s_flags;
+        meta[4] = meta[5] = meta[6] = meta[7] = 0;  // bin counter of the attention kernel
     }
 }
 
@@ -167,6 +156,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     __shared__ int s_scan[32];
     __shared__ unsigned s_flags;
     const int tid = threadIdx.x;
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (tid == 0) s_flags = 0;
     unsigned flags = 0;
     int N = 0;
@@ -200,12 +191,21 @@ __global__ void __launch_bounds__(kPlanThreads)
         meta[1] = S;
         meta[2] = bins;
         meta[3] = (int)s_flags;
+        meta[4] = meta[5] = meta[6] = meta[7] = 0;
     }
 }
 
 }  // namespace
 
 int assign_smem_bytes(int B) { return (B > 0 ? B : 1) * (int)sizeof(int); }
+
+// Smallest multiple of 32 threads covering the largest loop (capped at 1024):
+// small batches are planned by a few warps, with cheaper barriers.
+static int plan_threads(int B, int Hkv, int num_ctas) {
+    const long long work = max((long long)B * Hkv, (long long)num_ctas + 1);
+    const long long t = (work + 31) / 32 * 32;
+    return (int)min(max(t, 64LL), (long long)kPlanThreads);
+}
 
 cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages, int num_ctas,
                           int floor, const hpc_task_map &map, cudaStream_t s) {
@@ -215,10 +215,19 @@ cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
     }
-    assign_kernel<<<1, kPlanThreads, smem, s>>>(
-        seqlens, B, Hkv, max_pages, num_ctas, floor, reinterpret_cast<int4 *>(map.desc),
-        map.bin_ptr, map.chunk_count, map.chunk_off, map.meta, map.cap_desc);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(plan_threads(B, Hkv, num_ctas));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, assign_kernel, seqlens, B, Hkv, max_pages, num_ctas, floor,
+                              reinterpret_cast<int4 *>(map.desc), map.bin_ptr, map.chunk_count,
+                              map.chunk_off, map.meta, map.cap_desc);
 }
 
 cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_pages,

@@ -22,8 +22,11 @@ def device_ctas(kv_dtype: str) -> int:
 
 
 def run_step(batch: Batch, num_ctas: int | None = None, floor: int | None = None,
-             num_splits: int = 0):
-    """One plan + attention + combine through the C ABI; returns (out, workspace)."""
+             num_splits: int = 0, fused: bool = True):
+    """One plan + attention + combine through the C ABI; returns (out, workspace).
+
+    fused: the combine runs inside the attention grid (hpc_decode_attn_combine);
+    otherwise hpc_decode_attn is followed by the combine kernel."""
     w = batch.workload
     if num_ctas is None:
         num_ctas = w.num_ctas or device_ctas(w.kv_dtype)
@@ -35,8 +38,10 @@ def run_step(batch: Batch, num_ctas: int | None = None, floor: int | None = None
     hd.hpc_decode_step(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
                        batch.v_scale, batch.block_table, batch.seqlens, w.num_q_heads,
                        w.num_kv_heads, w.sm_scale, num_ctas, floor, num_splits, ws.tmap,
-                       ws.part_o, ws.part_lse, ws.out)
+                       ws.part_o, ws.part_lse, ws.out, unit_done=ws.unit_done if fused else None)
     torch.cuda.synchronize()
+    if fused:  # every launch must leave the chunk counters at zero
+        assert int(torch.count_nonzero(ws.unit_done)) == 0
     return ws.out[:B], ws
 
 

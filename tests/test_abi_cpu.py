@@ -49,7 +49,7 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced on the host
 
 def fake_map(hd, cap_desc=200, cap_bins=200, cap_units=64):
     m = hd.binding.hpc_task_map(FAKE, FAKE, FAKE, FAKE, FAKE, cap_desc, cap_bins, cap_units, 0, 0,
-                                0)
+                                0, 0, 0, 0)
     return m
 
 
@@ -133,3 +133,14 @@ def test_combine_argument_checks(hd):
 def test_status_strings(hd):
     assert hd.binding.status_string(0) == "ok"
     assert hd.binding.status_string(-3) == "workspace too small"
+
+
+def test_fused_attention_argument_checks(hd):
+    m = fake_map(hd)
+    m.B, m.Hkv, m.num_ctas = 4, 1, 132
+    L = hd.lib()
+    args = [FAKE, None, FAKE, FAKE, 10, 1.0, 1.0, 0, FAKE, 4, FAKE, 4, 8, 1, 128, 0.088,
+            ctypes.byref(m), FAKE, FAKE]
+    assert L.hpc_decode_attn_combine(*args, None, FAKE, None) == hd.binding.HPC_ERR_ARG
+    assert L.hpc_decode_attn_combine(*args, FAKE, None, None) == hd.binding.HPC_ERR_ARG
+    assert L.hpc_decode_attn_combine(*args, FAKE, FAKE + 8, None) == hd.binding.HPC_ERR_ARG

@@ -35,12 +35,74 @@ def test_tiny_workload_full_parity():
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("hq,hkv", [(8, 1), (8, 2), (16, 2), (4, 1), (1, 1), (64, 8), (6, 3)])
 @pytest.mark.parametrize("ctas", [1, 7, 0])
-def test_small_shapes(kv_dtype, hq, hkv, ctas):
+@pytest.mark.parametrize("fused", [True, False])
+def test_small_shapes(kv_dtype, hq, hkv, ctas, fused):
     w = small(len(BOUNDARY_LENS), hq, hkv, kv_dtype, ctas=ctas)
     batch = make_batch(w, device="cuda", seqlens=BOUNDARY_LENS, poison_tail=True,
                        seed=100 + hq + hkv)
-    out, _ = run_step(batch)
+    out, _ = run_step(batch, fused=fused)
     assert_close(out, oracle_out(batch), kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_fused_and_separate_combine_agree(kv_dtype):
+    lens = [9000, 3, 64, 700, 129, 20000, 0, 65]
+    w = small(len(lens), 8, 2, kv_dtype)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=17)
+    for ctas in (5, 33, 152):
+        a, _ = run_step(batch, num_ctas=ctas, fused=True)
+        b, _ = run_step(batch, num_ctas=ctas, fused=False)
+        assert (a.float() - b.float()).abs().max().item() <= 2 ** -8
+
+
+def test_fused_counters_survive_repeated_launches():
+    # the map is reused by several launches (layers); counters reset themselves
+    lens = [30000, 100, 5000, 64]
+    w = small(len(lens), 8, 1)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=23)
+    ws = hd.Workspace(4, 8, 1, num_ctas=40)
+    hd.hpc_decode_plan(batch.seqlens, 1, batch.max_pages, 40, 2, ws.tmap)
+    outs = []
+    for _ in range(3):
+        ws.out.fill_(float("nan"))
+        hd.hpc_decode_attn_combine(batch.q, None, batch.k_cache, batch.v_cache, 1.0, 1.0,
+                                   batch.block_table, batch.seqlens, 8, 1, w.sm_scale, ws.tmap,
+                                   ws.part_o, ws.part_lse, ws.unit_done, ws.out)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws.unit_done)) == 0
+        outs.append(ws.out.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    assert_close(outs[0], oracle_out(batch), "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("bins_per_cta", [2, 4])
+def test_dynamic_bins_parity_and_counter_reset(kv_dtype, bins_per_cta):
+    # more bins than resident CTAs: the persistent grid pulls the extra bins
+    lens = [20000, 5, 3000, 64, 129, 70000, 0, 640, 1]
+    w = small(len(lens), 8, 2, kv_dtype)
+    batch = make_batch(w, device="cuda", seqlens=lens, poison_tail=True, seed=41)
+    bins = bins_per_cta * device_ctas(kv_dtype) + 3
+    ws = hd.Workspace(len(lens), 8, 2, num_ctas=bins)
+    hd.hpc_decode_plan(batch.seqlens, 2, batch.max_pages, bins, 1, ws.tmap)
+    ref = oracle_out(batch)
+    outs = []
+    for _ in range(3):  # the map is reused; the bin counter must come back to zero
+        ws.out.fill_(float("nan"))
+        hd.hpc_decode_attn_combine(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
+                                   batch.k_scale, batch.v_scale, batch.block_table, batch.seqlens,
+                                   8, 2, w.sm_scale, ws.tmap, ws.part_o, ws.part_lse, ws.unit_done,
+                                   ws.out)
+        torch.cuda.synchronize()
+        meta = ws.tmap.meta.tolist()
+        assert meta[3] == 0 and meta[4] == 0
+        assert int(torch.count_nonzero(ws.unit_done)) == 0
+        outs.append(ws.out[:len(lens)].clone())
+    for o in outs:
+        assert_close(o, ref, kv_dtype)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    unfused, _ = run_step(batch, num_ctas=bins, floor=1, fused=False)
+    assert_close(unfused, ref, kv_dtype)
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
@@ -75,11 +137,12 @@ def test_constant_v_returns_that_row():
     assert err <= 2 ** -7 * 3  # one bf16 rounding of |row| <= 3
 
 
-def test_zero_length_requests_give_zero_rows():
+@pytest.mark.parametrize("fused", [True, False])
+def test_zero_length_requests_give_zero_rows(fused):
     lens = [0, 100, 0, 5000]
     w = small(4, 8, 1)
     batch = make_batch(w, device="cuda", seqlens=lens, seed=4)
-    out, _ = run_step(batch, num_ctas=9)
+    out, _ = run_step(batch, num_ctas=9, fused=fused)
     assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
     assert_close(out, oracle_out(batch), "bf16")
 
@@ -108,10 +171,11 @@ def test_deterministic_and_page_permutation_invariant(kv_dtype):
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("S", [1, 3, 8])
-def test_static_schedule_parity(kv_dtype, S):
+@pytest.mark.parametrize("fused", [True, False])
+def test_static_schedule_parity(kv_dtype, S, fused):
     w = small(len(BOUNDARY_LENS), 8, 2, kv_dtype)
     batch = make_batch(w, device="cuda", seqlens=BOUNDARY_LENS, poison_tail=True, seed=11)
-    out, ws = run_step(batch, num_splits=S)
+    out, ws = run_step(batch, num_splits=S, fused=fused)
     assert ws.tmap.to_host()["flags"] == 0
     assert_close(out, oracle_out(batch), kv_dtype)
 
@@ -130,7 +194,7 @@ def test_bad_page_is_flagged_not_read_out_of_bounds():
 def test_host_buffer_step_matches_device_step():
     w = WORKLOADS["tiny"]
     batch = make_batch(w, device="cuda")
-    dev_out, _ = run_step(batch)
+    dev_out, _ = run_step(batch, fused=False)
     B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
     h_q = batch.q.cpu().pin_memory()
     h_sl = batch.seqlens.cpu().pin_memory()
@@ -212,3 +276,31 @@ def test_table3_mixes_parity(name):
     assert_close(out, oracle_out(batch, rows=rows), "e4m3", rows=rows)
     static, _ = run_step(batch, num_splits=4)
     assert_close(static, oracle_out(batch, rows=rows), "e4m3", rows=rows)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_step_replays_from_a_cuda_graph(kv_dtype):
+    # the step's launches (incl. the programmatic dependent ones) can be captured
+    lens = [9000, 3, 640, 70000, 0, 129]
+    w = small(len(lens), 8, 2, kv_dtype)
+    batch = make_batch(w, device="cuda", seqlens=lens, seed=51)
+    eager, _ = run_step(batch, num_ctas=40, floor=2)
+    ws = hd.Workspace(len(lens), 8, 2, num_ctas=40)
+
+    def step():
+        hd.hpc_decode_step(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
+                           batch.v_scale, batch.block_table, batch.seqlens, 8, 2, w.sm_scale, 40,
+                           2, 0, ws.tmap, ws.part_o, ws.part_lse, ws.out, unit_done=ws.unit_done)
+
+    step()  # one-time set-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(2):
+        ws.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(ws.out[:len(lens)], eager)
+        assert int(torch.count_nonzero(ws.unit_done)) == 0

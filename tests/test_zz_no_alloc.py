@@ -31,7 +31,7 @@ def noalloc(batch, num_ctas, floor):
 def check_against_step(batch, num_ctas, floor):
     ref, ws = run_step(batch, num_ctas=num_ctas, floor=floor)
     got, meta = noalloc(batch, num_ctas, floor)
-    assert meta == ws.tmap.meta.tolist()
+    assert meta == ws.tmap.meta.tolist()[:4]
     assert meta[3] == 0
     err = (got.float() - ref.float()).abs()
     tol_max, tol_mean = TOL[batch.workload.kv_dtype]
