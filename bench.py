@@ -81,10 +81,10 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_src_hash):
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "attn_bf16_hy3_tp8.md")
+def profiled_traffic(kernel_src_hash, kv_dtype, workload):
+    """DRAM bytes per attention launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_{kv_dtype.replace('e4m3', 'fp8')}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -431,7 +431,7 @@ def main():
     mean_attn = statistics.fmean(attn_us_list)
     peak, peak_kind = measured_peaks()
     achieved = nbytes["attn_fused"] / (mean_attn * 1e-6) / 1e9
-    traffic = profiled_traffic(kernel_source_hash())
+    traffic = profiled_traffic(kernel_source_hash(), kv_dtype, w.name)
 
     # ---- the same step with the combine as its own kernel
     n_unf = min(args.steps, 1000)
