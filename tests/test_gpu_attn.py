@@ -304,3 +304,30 @@ def test_step_replays_from_a_cuda_graph(kv_dtype):
         torch.cuda.synchronize()
         assert torch.equal(ws.out[:len(lens)], eager)
         assert int(torch.count_nonzero(ws.unit_done)) == 0
+
+
+def test_randomized_stress_against_oracle():
+    # random shapes, lengths, floors and bin counts; fused and separate combine;
+    # every case is checked against the oracle and re-run for bitwise equality
+    rng = np.random.default_rng(2026)
+    for case in range(30):
+        kv_dtype = "e4m3" if rng.random() < 0.5 else "bf16"
+        hkv = int(rng.choice([1, 2, 4]))
+        hq = hkv * int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.integers(1, 24))
+        lens = []
+        for _ in range(B):
+            kind = rng.random()
+            lens.append(int(rng.integers(0, 3)) if kind < 0.1 else
+                        int(rng.integers(1, 300)) if kind < 0.5 else
+                        int(2 ** rng.uniform(8, 15)))
+        floor = int(rng.choice([0, 1, 2, 8]))
+        ctas = int(rng.choice([1, 13, 100, device_ctas(kv_dtype), 3 * device_ctas(kv_dtype) + 1]))
+        fused = bool(rng.random() < 0.7)
+        w = small(B, hq, hkv, kv_dtype, floor=floor)
+        batch = make_batch(w, device="cuda", seqlens=lens, poison_tail=True, seed=500 + case)
+        a, ws = run_step(batch, num_ctas=ctas, floor=floor, fused=fused)
+        assert ws.tmap.to_host()["flags"] == 0
+        b, _ = run_step(batch, num_ctas=ctas, floor=floor, fused=fused)
+        assert torch.equal(a, b), f"case {case} not deterministic"
+        assert_close(a, oracle_out(batch), kv_dtype)
