@@ -20,6 +20,13 @@
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  Launch sizes depend only on
  *     host-known bounds, never on device data.
+ *   - Kernels are launched as programmatic dependents of the previous kernel
+ *     on the stream: they may become resident while it still runs, but none
+ *     reads or writes caller data before that kernel has finished, with one
+ *     exception internal to hpc_decode_step (and the entry points built on
+ *     it): there the attention grid starts streaming its first tiles while
+ *     the assign kernel it follows, which itself waited for everything
+ *     before it, is still running.
  *   - The returned status covers host-side argument checks and the launch
  *     itself (cudaGetLastError).  Problems only visible on the device (bad
  *     seqlens, block-table entries out of range, a wait that timed out) are
@@ -319,6 +326,79 @@ hpc_status hpc_decode_step_noalloc(const void *d_q, const float *d_q_scale, cons
                                    int32_t head_dim, float sm_scale, int32_t num_ctas,
                                    int32_t min_tiles_per_cta, void *d_out, int32_t *d_meta_out,
                                    hpc_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Fused attention prologue (HpcRopeNorm).
+ *
+ * vLLM integration post, "A fused attention prologue"; SGLang post, the
+ * paragraph on the Hy3 FP8 prologue: starting from the fused QKV projection
+ * of the new tokens, one kernel applies QK-Norm and RoPE in the model's
+ * order (Hy3 normalises first), writes K and V straight into the paged
+ * cache and, for FP8, emits the query as E4M3 with one scale per
+ * (token, head), which hpc_decode_attn takes as it is (q, q_scale).
+ *
+ * The posts give no constants; the op takes them as parameters and uses
+ * the standard definitions:
+ *   RMS norm of a head row x:  x / sqrt(mean(x^2) + eps) * w, with one BF16
+ *     weight vector w[128] for all query heads and one for all key heads;
+ *   RoPE over the whole head: frequency i < 64 is base^(-2i/128); the pair
+ *     (a, b) turns by pos * freq_i into (a cos - b sin, b cos + a sin);
+ *     pairs are (i, i + 64) for HPC_ROPE_HALVES, (2i, 2i + 1) for
+ *     HPC_ROPE_INTERLEAVED;
+ *   V is not normalised or rotated;
+ *   FP8 query: scale = amax / 448 over the head row (1 for an all-zero
+ *     row), codes = E4M3 round-to-nearest-even of y / scale (saturating);
+ *   FP8 K and V: E4M3 of y / k_scale and v / v_scale (saturating).
+ * The arithmetic is fp32; the rotation angle is reduced modulo 2 pi in fp64,
+ * so long positions keep their accuracy.
+ * ---------------------------------------------------------------------- */
+typedef enum { HPC_ROPE_HALVES = 0, HPC_ROPE_INTERLEAVED = 1 } hpc_rope_layout;
+
+typedef struct {
+    float eps;           /* RMS-norm epsilon, finite, >= 0 */
+    float rope_base;     /* RoPE base, finite, > 0 */
+    int32_t rope_layout; /* hpc_rope_layout */
+    int32_t norm_first;  /* 1: QK-Norm then RoPE (Hy3); 0: RoPE then QK-Norm */
+} hpc_rope_norm_params;
+
+/*
+ * Runs the prologue for num_tokens new tokens.
+ *   d_qkv          device bf16 [num_tokens, qkv_row_stride]; a token's row
+ *                  holds Hq query heads, then Hkv key heads, then Hkv value
+ *                  heads, 128 elements each; qkv_row_stride (elements) is
+ *                  >= (Hq + 2 Hkv) * 128 and a multiple of 8
+ *   d_q_norm_w, d_k_norm_w  device bf16 [128]
+ *   d_positions    device int32 [num_tokens]: the token's position in its
+ *                  request, which is both its RoPE position and its cache slot
+ *   d_token_req    device int32 [num_tokens] (the token's request) or NULL,
+ *                  meaning token t belongs to request t (decode)
+ *   d_block_table  device int32 [B, max_pages_per_req]
+ *   d_k_cache, d_v_cache  device [num_pages, 64, Hkv, 128] of kv_dtype;
+ *                  token t of request r at position p is written to page
+ *                  block_table[r, p / 64], slot p % 64; nothing else changes
+ *   d_q_out        device [num_tokens, Hq, 128]: bf16 (BF16 KV) or e4m3 (FP8 KV)
+ *   d_q_scale_out  device fp32 [num_tokens, Hq]: FP8 only (NULL for BF16)
+ *   d_flags        device int32 or NULL: OR-ed with HPC_FLAG_BAD_SEQLEN when
+ *                  a token's request or position is out of range and with
+ *                  HPC_FLAG_BAD_PAGE when its page is outside [0, num_pages);
+ *                  such a token still gets its query but writes no cache slot
+ * All device pointers 16-byte aligned; the caller owns every buffer.  Two
+ * tokens that name the same cache slot leave either one's row there.
+ * Asynchronous on `stream`.  The kernel waits for the preceding kernel on
+ * the stream to finish before it reads anything (it may be launched early
+ * as a programmatic dependent of it) and lets its own dependents start only
+ * when it has finished, so an attention launch that follows sees the new
+ * cache rows.  Returns HPC_ERR_ARG / HPC_ERR_UNSUPPORTED on bad arguments
+ * (head_dim != 128, Hq % Hkv != 0), HPC_ERR_CUDA if the launch fails.
+ */
+hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride, const void *d_q_norm_w,
+                         const void *d_k_norm_w, const int32_t *d_positions,
+                         const int32_t *d_token_req, int32_t num_tokens, int32_t Hq, int32_t Hkv,
+                         int32_t head_dim, const int32_t *d_block_table,
+                         int32_t max_pages_per_req, int32_t B, void *d_k_cache, void *d_v_cache,
+                         int32_t num_pages, hpc_kv_dtype kv_dtype, float k_scale, float v_scale,
+                         void *d_q_out, float *d_q_scale_out, int32_t *d_flags,
+                         const hpc_rope_norm_params *params, hpc_stream_t stream);
 
 /*
  * Synchronises `stream` and copies map->meta into host_meta[4]

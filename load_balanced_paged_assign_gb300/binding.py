@@ -19,13 +19,14 @@ HPC_OK, HPC_ERR_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_WORKSPACE, HPC_ERR_CUDA = 0, -
 HPC_KV_BF16, HPC_KV_FP8_E4M3 = 0, 1
 HPC_FLAG_BAD_SEQLEN, HPC_FLAG_DESC_OVERFLOW, HPC_FLAG_BAD_PAGE, HPC_FLAG_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, PAGE_SIZE, MAX_GROUP = 128, 64, 8
+HPC_ROPE_HALVES, HPC_ROPE_INTERLEAVED = 0, 1
 
 # Every symbol the header declares; the CPU tests check the library exports them all.
 EXPORTS = (
     "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
     "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
-    "hpc_decode_step_noalloc",
+    "hpc_decode_step_noalloc", "hpc_rope_norm",
 )
 
 
@@ -45,6 +46,11 @@ class hpc_task_map(ctypes.Structure):
         ("persistent", ctypes.c_int32), ("min_tiles", ctypes.c_int32),
         ("max_pages", ctypes.c_int32),
     ]
+
+
+class hpc_rope_norm_params(ctypes.Structure):
+    _fields_ = [("eps", ctypes.c_float), ("rope_base", ctypes.c_float),
+                ("rope_layout", ctypes.c_int32), ("norm_first", ctypes.c_int32)]
 
 
 _LIB = None
@@ -92,6 +98,9 @@ def lib():
         "hpc_decode_step_noalloc": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
                                                    vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
                                                    vp, vp, vp]),
+        "hpc_rope_norm": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, vp, i32,
+                                         i32, vp, vp, i32, ctypes.c_int, f32, f32, vp, vp, vp,
+                                         ctypes.POINTER(hpc_rope_norm_params), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -281,6 +290,21 @@ def hpc_decode_step_noalloc(q, q_scale, k_cache, v_cache, k_scale, v_scale, bloc
         int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
         HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta), _ptr(out),
         _ptr(meta_out), _stream(stream)))
+
+
+def hpc_rope_norm(qkv, q_norm_w, k_norm_w, positions, token_req, Hq, Hkv, block_table, k_cache,
+                  v_cache, k_scale, v_scale, q_out, q_scale_out=None, flags=None, *, eps=1e-6,
+                  rope_base=1e6, rope_layout=HPC_ROPE_HALVES, norm_first=True, stream=None):
+    """Fused prologue: QK-Norm + RoPE of the new tokens' heads, K/V written into
+    the paged cache, the query into q_out (and q_scale_out for FP8)."""
+    params = hpc_rope_norm_params(float(eps), float(rope_base), int(rope_layout),
+                                  1 if norm_first else 0)
+    _check("hpc_rope_norm", lib().hpc_rope_norm(
+        _ptr(qkv), int(qkv.stride(0)), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions),
+        _ptr(token_req), int(positions.numel()), int(Hq), int(Hkv), HEAD_DIM, _ptr(block_table),
+        int(block_table.shape[1]), int(block_table.shape[0]), _ptr(k_cache), _ptr(v_cache),
+        int(k_cache.shape[0]), kv_dtype_of(k_cache), float(k_scale), float(v_scale), _ptr(q_out),
+        _ptr(q_scale_out), _ptr(flags), ctypes.byref(params), _stream(stream)))
 
 
 class Workspace:

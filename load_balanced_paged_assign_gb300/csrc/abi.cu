@@ -137,7 +137,8 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
                             int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
                             int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                             const hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                            int32_t *d_unit_done, void *d_out, hpc_stream_t stream) {
+                            int32_t *d_unit_done, void *d_out, bool after_plan,
+                            hpc_stream_t stream) {
     hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
     if (st != HPC_OK) return st;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
@@ -196,12 +197,34 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
     p.num_bins = map->num_ctas;
     p.bin_counter = map->meta + 4;
     p.min_tiles = map->min_tiles;
-    // the first descriptor is derived in-kernel only for a load-balanced map
-    // planned against this very block-table shape
-    p.fly = map->persistent && map->max_pages == max_pages_per_req ? 1 : 0;
+    // The first descriptor is derived in-kernel, and streamed before the grid
+    // waits on its predecessor, only right behind this library's own assign
+    // kernel: that kernel waited for everything before it, so the caller's
+    // inputs are complete.  Behind any other kernel (a reused map) every read
+    // waits.  The map must be load-balanced and planned for this block table.
+    p.fly = after_plan && map->persistent && map->max_pages == max_pages_per_req ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = fp8 ? launch_attn_fp8(tk, tv, p, grid, s) : launch_attn_bf16(tk, tv, p, grid, s);
     return cuda_status(e);
+}
+
+// hpc_decode_attn_combine's checks and launch; after_plan as in launch_attention.
+hpc_status attn_combine(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                        const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                        hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                        int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                        int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                        const hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                        int32_t *d_unit_done, void *d_out, bool after_plan,
+                        hpc_stream_t stream) {
+    if (B > 0 && (!d_unit_done || !d_out)) return HPC_ERR_ARG;
+    if (!aligned16(d_out)) return HPC_ERR_ARG;
+    if (!map || !map->chunk_count || !map->chunk_off) return HPC_ERR_ARG;
+    if ((int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
+    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                            head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
+                            after_plan, stream);
 }
 
 }  // namespace
@@ -311,7 +334,7 @@ hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *
     return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                             kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                             head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr,
-                            stream);
+                            false, stream);
 }
 
 hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, const void *d_k_cache,
@@ -322,14 +345,10 @@ hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, cons
                                    int32_t head_dim, float sm_scale, const hpc_task_map *map,
                                    float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
                                    void *d_out, hpc_stream_t stream) {
-    if (B > 0 && (!d_unit_done || !d_out)) return HPC_ERR_ARG;
-    if (!aligned16(d_out)) return HPC_ERR_ARG;
-    if (!map || !map->chunk_count || !map->chunk_off) return HPC_ERR_ARG;
-    if ((int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
-    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
-                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
-                            head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
-                            stream);
+    return attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                        kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                        head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out, false,
+                        stream);
 }
 
 hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
@@ -362,14 +381,16 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
                          : hpc_decode_plan_static(d_seqlens, B, Hkv, max_pages_per_req,
                                                   num_splits, map, stream);
     if (st != HPC_OK) return st;
+    // the attention grid follows the assign kernel directly (after_plan)
     if (d_unit_done)  // fused: the attention grid also performs the combine
-        return hpc_decode_attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale,
-                                       v_scale, kv_dtype, d_block_table, max_pages_per_req,
-                                       d_seqlens, B, Hq, Hkv, head_dim, sm_scale, map, d_part_o,
-                                       d_part_lse, d_unit_done, d_out, stream);
-    st = hpc_decode_attn(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
-                         kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
-                         head_dim, sm_scale, map, d_part_o, d_part_lse, stream);
+        return attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                            head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
+                            true, stream);
+    st = launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                          kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                          head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr, true,
+                          stream);
     if (st != HPC_OK) return st;
     return hpc_decode_combine(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, d_out, stream);
 }

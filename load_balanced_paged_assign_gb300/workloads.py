@@ -212,3 +212,119 @@ def _poison_tails(k, v, bt, lens):
                 t.view(torch.uint8)[page, L % PAGE:] = 0x7F
             else:
                 t[page, L % PAGE:] = float("nan")
+
+
+# ---------------------------------------------------------------- prologue
+# Inputs of the fused attention prologue (QK-Norm, RoPE, paged KV write, FP8
+# query), which produces the decode path's Q and the new token's cache rows.
+# The pages give its shapes (the Hy3 head layout) but none of its constants:
+# RoPE base, epsilon and norm weights are synthetic.
+#
+# Recipe: the fused QKV rows are N(0, 1) draws; each query and key head row
+# is multiplied by its own magnitude, log-uniform on [1/4, 8], so that the
+# norm has something to undo (value rows keep unit scale); the norm weights
+# are 1 + N(0, 1)/4; all rounded to BF16.  Decode: one new token per request
+# of a decode workload, at position L_r - 1 of that request's pages (it
+# overwrites the slot the batch drew there).  Prefill: one request of N
+# tokens at positions 0..N-1 over a shuffled page list, the caches starting
+# at zero; FP8 cache scales are fixed at 8/448 for K (normalised rows stay
+# within about 8) and amax(V)/448 for V.
+
+
+@dataclass(frozen=True)
+class PrologueWorkload:
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    kv_dtype: str = "bf16"
+    decode_of: str = ""  # decode: one new token per request of this decode workload
+    prefill_tokens: int = 0  # prefill: one request of this many tokens
+    rope_base: float = 1e6
+    eps: float = 1e-6
+    rope_layout: int = 0  # 0: pairs (i, i + 64); 1: pairs (2i, 2i + 1)
+    norm_first: bool = True
+    seed: int = 1200
+    description: str = ""
+
+
+PROLOGUES = {
+    "decode_hy3_tp8": PrologueWorkload(
+        "decode_hy3_tp8", 8, 1, decode_of="hy3_tp8", seed=1201,
+        description="prologue of one decode step of hy3_tp8: 32 tokens, Hq=8, Hkv=1, BF16"),
+    "decode_fp8": PrologueWorkload(
+        "decode_fp8", 8, 1, kv_dtype="e4m3", decode_of="fp8", seed=1202,
+        description="prologue of one decode step of the FP8 workload: 64 tokens, Hq=8, Hkv=1"),
+    "prefill_8k_fp8": PrologueWorkload(
+        "prefill_8k_fp8", 64, 8, kv_dtype="e4m3", prefill_tokens=8192, seed=1203,
+        description="8K-token prefill prologue at the Hy3 TP1 head shape (Hq=64, Hkv=8), FP8"),
+    "prefill_8k_bf16": PrologueWorkload(
+        "prefill_8k_bf16", 64, 8, prefill_tokens=8192, seed=1204,
+        description="8K-token prefill prologue at the Hy3 TP1 head shape (Hq=64, Hkv=8), BF16"),
+}
+
+
+@dataclass
+class PrologueInputs:
+    workload: PrologueWorkload
+    qkv: torch.Tensor  # bf16 [N, (Hq + 2 Hkv) * 128]
+    q_norm_w: torch.Tensor  # bf16 [128]
+    k_norm_w: torch.Tensor  # bf16 [128]
+    positions: torch.Tensor  # int32 [N]
+    token_req: torch.Tensor | None  # int32 [N], or None: token t is request t
+    block_table: torch.Tensor  # int32 [B, max_pages]
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: float
+    v_scale: float
+    batch: Batch | None = None  # the decode batch whose caches are written
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.positions.numel())
+
+
+def draw_qkv(N: int, Hq: int, Hkv: int, seed: int, device) -> tuple:
+    """(qkv bf16 [N, (Hq + 2 Hkv) * 128], q_norm_w, k_norm_w) per the recipe above."""
+    gen = torch.Generator().manual_seed(seed)
+    R = Hq + 2 * Hkv
+    mag = torch.exp(torch.empty((N, Hq + Hkv, 1)).uniform_(math.log(0.25), math.log(8.0),
+                                                           generator=gen))
+    mag = torch.cat([mag, torch.ones((N, Hkv, 1))], dim=1)
+    rows = _normal((N, R, HEAD_DIM), seed + 1, device) * mag.to(device)
+    qkv = rows.to(torch.bfloat16).reshape(N, R * HEAD_DIM)
+    wq = (1.0 + 0.25 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16).to(device)
+    wk = (1.0 + 0.25 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16).to(device)
+    return qkv, wq, wk
+
+
+def make_prologue_inputs(pw: PrologueWorkload, device="cpu", seed: int | None = None,
+                         seqlens: list | None = None) -> PrologueInputs:
+    seed = pw.seed if seed is None else seed
+    Hq, Hkv = pw.num_q_heads, pw.num_kv_heads
+    if pw.decode_of:
+        w = WORKLOADS[pw.decode_of]
+        batch = make_batch(w, device=device, seqlens=seqlens)
+        N = int(batch.seqlens.numel())
+        qkv, wq, wk = draw_qkv(N, Hq, Hkv, seed, device)
+        positions = (batch.seqlens - 1).to(torch.int32)
+        return PrologueInputs(pw, qkv, wq, wk, positions, None, batch.block_table,
+                              batch.k_cache, batch.v_cache, batch.k_scale, batch.v_scale, batch)
+    N = pw.prefill_tokens
+    gen = torch.Generator().manual_seed(seed + 7)
+    pages = (N + PAGE - 1) // PAGE
+    bt = torch.randperm(pages, generator=gen).to(torch.int32).reshape(1, pages).to(device)
+    qkv, wq, wk = draw_qkv(N, Hq, Hkv, seed, device)
+    shape = (pages, PAGE, Hkv, HEAD_DIM)
+    fp8 = pw.kv_dtype == "e4m3"
+    dtype = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    k_cache = torch.zeros(shape, dtype=dtype, device=device)
+    v_cache = torch.zeros(shape, dtype=dtype, device=device)
+    k_scale = v_scale = 1.0
+    if fp8:
+        k_scale = 8.0 / 448.0
+        v_rows = qkv.reshape(N, Hq + 2 * Hkv, HEAD_DIM)[:, Hq + Hkv:]
+        v_scale = float(v_rows.float().abs().max().item()) / 448.0
+    positions = torch.arange(N, dtype=torch.int32, device=device)
+    token_req = torch.zeros(N, dtype=torch.int32, device=device)
+    return PrologueInputs(pw, qkv, wq, wk, positions, token_req, bt, k_cache, v_cache, k_scale,
+                          v_scale)

@@ -144,3 +144,34 @@ def test_fused_attention_argument_checks(hd):
     assert L.hpc_decode_attn_combine(*args, None, FAKE, None) == hd.binding.HPC_ERR_ARG
     assert L.hpc_decode_attn_combine(*args, FAKE, None, None) == hd.binding.HPC_ERR_ARG
     assert L.hpc_decode_attn_combine(*args, FAKE, FAKE + 8, None) == hd.binding.HPC_ERR_ARG
+
+
+def call_rope_norm(hd, qkv=FAKE, stride=1280, N=4, Hq=8, Hkv=1, D=128, B=4, dtype=0,
+                   q_scale=None, qout=FAKE, params="default", token_req=None, k_scale=1.0):
+    P = hd.binding.hpc_rope_norm_params
+    p = P(1e-6, 1e6, 0, 1) if params == "default" else params
+    return hd.lib().hpc_rope_norm(qkv, stride, FAKE, FAKE, FAKE, token_req, N, Hq, Hkv, D, FAKE,
+                                  16, B, FAKE, FAKE, 10, dtype, k_scale, 1.0, qout, q_scale, None,
+                                  None if p is None else ctypes.byref(p), None)
+
+
+def test_rope_norm_argument_checks(hd):
+    E = hd.binding
+    P = E.hpc_rope_norm_params
+    assert call_rope_norm(hd, N=0) == E.HPC_OK  # nothing to do, nothing launched
+    assert call_rope_norm(hd, params=None) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, D=64) == E.HPC_ERR_UNSUPPORTED
+    assert call_rope_norm(hd, Hq=12, Hkv=8) == E.HPC_ERR_UNSUPPORTED
+    assert call_rope_norm(hd, stride=1272) == E.HPC_ERR_ARG  # shorter than a token's heads
+    assert call_rope_norm(hd, stride=1284) == E.HPC_ERR_ARG  # not a multiple of 8 elements
+    assert call_rope_norm(hd, qkv=FAKE + 8) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, dtype=1) == E.HPC_ERR_ARG  # FP8 without q_scale_out
+    assert call_rope_norm(hd, dtype=1, q_scale=FAKE, k_scale=0.0) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, dtype=5) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, N=5, B=4) == E.HPC_ERR_ARG  # token t is request t: needs N <= B
+    assert call_rope_norm(hd, qout=None) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(-1.0, 1e6, 0, 1)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 0.0, 0, 1)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, float("inf"), 0, 1)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 1e6, 2, 1)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 1e6, 0, 2)) == E.HPC_ERR_ARG
