@@ -70,6 +70,17 @@ def aggregate(per_rank_us, per_rank_bytes):
     return t, sum(per_rank_bytes) / (t * 1e-6) / 1e9
 
 
+def prologue_bytes(N, Hq, Hkv, kv_dtype):
+    """Bytes the fused prologue must move for N tokens: the fused QKV rows in,
+    the query (+ fp32 scales for FP8) and the new K and V cache rows out, plus
+    each token's position and block-table entry and the two norm weights."""
+    bpe = 1 if kv_dtype == "e4m3" else 2
+    read = N * (Hq + 2 * Hkv) * 128 * 2 + N * 8 + 2 * 128 * 2
+    write = N * Hq * 128 * bpe + (N * Hq * 4 if kv_dtype == "e4m3" else 0) + \
+        N * 2 * Hkv * 128 * bpe
+    return read + write
+
+
 # ------------------------------------------------------------------ environment
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -222,6 +233,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-static", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prologue", action="store_true")
     ap.add_argument("--floor", type=int, default=None)
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
@@ -341,8 +353,12 @@ def main():
             hd.hpc_decode_combine(w_s.part_o, w_s.part_lse, w_s.tmap, B, Hq, Hkv, w_s.out)
 
     def step(w_s, num_splits=0, fused=True):
-        plan(w_s.tmap, num_splits)
-        attention(w_s, fused)
+        """One decode step through the public step call: the assign kernel, then
+        the attention grid right behind it (fused combine unless fused=False)."""
+        hd.hpc_decode_step(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
+                           batch.v_scale, batch.block_table, batch.seqlens, Hq, Hkv, w.sm_scale,
+                           ctas, floor, num_splits, w_s.tmap, w_s.part_o, w_s.part_lse, w_s.out,
+                           unit_done=w_s.unit_done if fused else None)
 
     def graphed(fn):
         """fn captured once into a CUDA graph (the programmatic launch edges between
@@ -410,7 +426,9 @@ def main():
 
     # ---- the dominant kernel alone, as every layer runs it on the step's map:
     # flush, rebuild the map (untimed, so it sits in L2 as in a model where all
-    # layers share it), then time the attention launch by itself
+    # layers share it), then time the attention launch by itself (a standalone
+    # launch on a reused map, which reads nothing before the kernel ahead of
+    # it has finished)
     def attn_alone(n_steps, n_warm, w_s, num_splits=0):
         for _ in range(n_warm):
             flush.fill_(1)
@@ -486,6 +504,77 @@ def main():
                   "dynamic_speedup_vs_best_static": results[best][0] / mean_step,
                   "dynamic_attn_speedup_vs_best_static": results[best][1] / mean_attn}
 
+    # ---- the fused attention prologue: this step's new tokens, then the
+    # prologue followed by the per-layer attention on its outputs, then the
+    # HBM-bound 8K-token prefill shape against the roofline
+    prologue = None
+    if not args.no_prologue:
+        from load_balanced_paged_assign_gb300.workloads import (PROLOGUES, PrologueInputs,
+                                                                draw_qkv, make_prologue_inputs)
+
+        freq_tables = {}
+
+        def prologue_call(inp, q_out, q_scale_out):
+            pw_ = inp.workload
+            if pw_.rope_base not in freq_tables:  # built once, as a model keeps it
+                f = torch.empty(64, dtype=torch.float64, device=dev)
+                hd.hpc_rope_frequencies(pw_.rope_base, f)
+                freq_tables[pw_.rope_base] = f
+            hd.hpc_rope_norm(inp.qkv, inp.q_norm_w, inp.k_norm_w, inp.positions, inp.token_req,
+                             pw_.num_q_heads, pw_.num_kv_heads, inp.block_table, inp.k_cache,
+                             inp.v_cache, inp.k_scale, inp.v_scale, q_out, q_scale_out,
+                             eps=pw_.eps, rope_base=pw_.rope_base, rope_layout=pw_.rope_layout,
+                             norm_first=pw_.norm_first, freq=freq_tables[pw_.rope_base])
+
+        def outputs_for(inp):
+            pw_ = inp.workload
+            n = inp.num_tokens
+            qdt = torch.float8_e4m3fn if pw_.kv_dtype == "e4m3" else torch.bfloat16
+            q_o = torch.empty((n, pw_.num_q_heads, 128), dtype=qdt, device=dev)
+            qs_o = (torch.empty((n, pw_.num_q_heads), device=dev)
+                    if pw_.kv_dtype == "e4m3" else None)
+            return q_o, qs_o
+
+        n_pro = min(args.steps, 500)
+        prologue = {"launches_per_call": 1}
+        pw = next((p for p in PROLOGUES.values() if p.decode_of == w.name), None)
+        if pw is not None:
+            qkv, wq, wk = draw_qkv(B, Hq, Hkv, pw.seed, dev)
+            inp = PrologueInputs(pw, qkv, wq, wk, (batch.seqlens - 1).to(torch.int32), None,
+                                 batch.block_table, batch.k_cache, batch.v_cache, batch.k_scale,
+                                 batch.v_scale, batch)
+            q_o, qs_o = outputs_for(inp)
+            dec_us = statistics.fmean(timed(n_pro, args.warmup,
+                                            lambda: prologue_call(inp, q_o, qs_o)))
+
+            def layer():  # prologue, then the attention on its query and cache rows
+                prologue_call(inp, q_o, qs_o)
+                hd.hpc_decode_attn_combine(q_o, qs_o, batch.k_cache, batch.v_cache,
+                                           batch.k_scale, batch.v_scale, batch.block_table,
+                                           batch.seqlens, Hq, Hkv, w.sm_scale, ws.tmap,
+                                           ws.part_o, ws.part_lse, ws.unit_done, ws.out)
+
+            plan(ws.tmap)
+            layer_us = statistics.fmean(timed(n_pro, args.warmup, layer))
+            prologue["decode"] = {"workload": pw.name, "tokens": B, "us": dec_us,
+                                  "bytes": prologue_bytes(B, Hq, Hkv, kv_dtype),
+                                  "layer_us": layer_us,
+                                  "layer": "prologue + attention with fused combine on the "
+                                           "step's task map (two launches)"}
+        pre = PROLOGUES["prefill_8k_fp8"]
+        inp = make_prologue_inputs(pre, device=dev)
+        q_o, qs_o = outputs_for(inp)
+        pre_us = statistics.fmean(timed(n_pro, args.warmup, lambda: prologue_call(inp, q_o, qs_o)))
+        pre_bytes = prologue_bytes(inp.num_tokens, pre.num_q_heads, pre.num_kv_heads,
+                                   pre.kv_dtype)
+        pre_gbs = pre_bytes / (pre_us * 1e-6) / 1e9
+        prologue["prefill"] = {
+            "workload": pre.name, "description": pre.description, "tokens": inp.num_tokens,
+            "us": pre_us, "bytes": pre_bytes,
+            "roofline": {"bound": "hbm", "achieved": pre_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": pre_gbs / peak, "peak_kind": peak_kind}}
+        del inp, q_o, qs_o
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
@@ -517,6 +606,7 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu_baseline,
         "static": static,
+        "rope_norm": prologue,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }

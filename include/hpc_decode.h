@@ -16,7 +16,8 @@
  *   - All pointers named d_* or documented as "device" are CUDA device
  *     pointers owned by the caller.  The library never allocates or frees
  *     memory, never synchronises a stream (except hpc_decode_read_meta) and
- *     keeps no state between calls except a cached driver entry point.
+ *     keeps no state between calls except a cached driver entry point and
+ *     per-device launch facts (kernel attributes set, resident CTAs).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  Launch sizes depend only on
  *     host-known bounds, never on device data.
@@ -349,8 +350,11 @@ hpc_status hpc_decode_step_noalloc(const void *d_q, const float *d_q_scale, cons
  *   FP8 query: scale = amax / 448 over the head row (1 for an all-zero
  *     row), codes = E4M3 round-to-nearest-even of y / scale (saturating);
  *   FP8 K and V: E4M3 of y / k_scale and v / v_scale (saturating).
- * The arithmetic is fp32; the rotation angle is reduced modulo 2 pi in fp64,
- * so long positions keep their accuracy.
+ * The arithmetic is fp32.  The rotation angle pos * freq is formed as an
+ * exact fp32 product plus its rounding error against an fp64 frequency and
+ * reduced modulo 2 pi in extended precision, so every position below 2^24
+ * keeps an angle error of a few 1e-7 rad; max_pages_per_req * 64 must not
+ * exceed 2^24 (HPC_ERR_UNSUPPORTED).
  * ---------------------------------------------------------------------- */
 typedef enum { HPC_ROPE_HALVES = 0, HPC_ROPE_INTERLEAVED = 1 } hpc_rope_layout;
 
@@ -359,7 +363,18 @@ typedef struct {
     float rope_base;     /* RoPE base, finite, > 0 */
     int32_t rope_layout; /* hpc_rope_layout */
     int32_t norm_first;  /* 1: QK-Norm then RoPE (Hy3); 0: RoPE then QK-Norm */
+    const double *freq;  /* device fp64 [64] from hpc_rope_frequencies(rope_base), 16-byte
+                            aligned, or NULL: every CTA then builds the table itself in fp64,
+                            which costs a couple of microseconds at the start of the kernel */
 } hpc_rope_norm_params;
+
+/*
+ * Writes the 64 RoPE frequencies rope_base^(-2i/128), i = 0..63, in fp64 into
+ * d_freq (device, 16-byte aligned, caller-owned): the table a model builds
+ * once and passes to every hpc_rope_norm call through params->freq.
+ * Asynchronous on `stream`; HPC_ERR_ARG for a non-positive or non-finite base.
+ */
+hpc_status hpc_rope_frequencies(float rope_base, double *d_freq, hpc_stream_t stream);
 
 /*
  * Runs the prologue for num_tokens new tokens.

@@ -13,7 +13,8 @@ from .binding import (EXPORTS, HPC_KV_BF16, HPC_KV_FP8_E4M3, HPC_ROPE_HALVES,
                       hpc_decode_attn_combine, hpc_decode_combine, hpc_decode_desc_capacity,
                       hpc_decode_num_ctas, hpc_decode_plan, hpc_decode_plan_static,
                       hpc_decode_read_meta, hpc_decode_static_capacity, hpc_decode_step,
-                      hpc_decode_step_host, hpc_decode_version, hpc_rope_norm, kv_dtype_of, lib)
+                      hpc_decode_step_host, hpc_decode_version, hpc_rope_frequencies, hpc_rope_norm,
+                      kv_dtype_of, lib)
 
 __all__ = [
     "EXPORTS", "HPC_KV_BF16", "HPC_KV_FP8_E4M3", "HPC_ROPE_HALVES", "HPC_ROPE_INTERLEAVED",
@@ -21,5 +22,5 @@ __all__ = [
     "hpc_decode_combine", "hpc_decode_desc_capacity", "hpc_decode_num_ctas",
     "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_read_meta",
     "hpc_decode_static_capacity", "hpc_decode_step", "hpc_decode_step_host",
-    "hpc_decode_version", "hpc_rope_norm", "kv_dtype_of", "lib",
+    "hpc_decode_version", "hpc_rope_frequencies", "hpc_rope_norm", "kv_dtype_of", "lib",
 ]

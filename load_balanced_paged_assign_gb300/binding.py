@@ -26,7 +26,7 @@ EXPORTS = (
     "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
     "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
-    "hpc_decode_step_noalloc", "hpc_rope_norm",
+    "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies",
 )
 
 
@@ -50,7 +50,8 @@ class hpc_task_map(ctypes.Structure):
 
 class hpc_rope_norm_params(ctypes.Structure):
     _fields_ = [("eps", ctypes.c_float), ("rope_base", ctypes.c_float),
-                ("rope_layout", ctypes.c_int32), ("norm_first", ctypes.c_int32)]
+                ("rope_layout", ctypes.c_int32), ("norm_first", ctypes.c_int32),
+                ("freq", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -98,6 +99,7 @@ def lib():
         "hpc_decode_step_noalloc": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
                                                    vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
                                                    vp, vp, vp]),
+        "hpc_rope_frequencies": (ctypes.c_int, [f32, vp, vp]),
         "hpc_rope_norm": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, vp, i32,
                                          i32, vp, vp, i32, ctypes.c_int, f32, f32, vp, vp, vp,
                                          ctypes.POINTER(hpc_rope_norm_params), vp]),
@@ -292,13 +294,22 @@ def hpc_decode_step_noalloc(q, q_scale, k_cache, v_cache, k_scale, v_scale, bloc
         _ptr(meta_out), _stream(stream)))
 
 
+def hpc_rope_frequencies(rope_base, freq, stream=None):
+    """The fp64 RoPE frequency table [64] for rope_base, written into `freq`."""
+    _check("hpc_rope_frequencies",
+           lib().hpc_rope_frequencies(float(rope_base), _ptr(freq), _stream(stream)))
+
+
 def hpc_rope_norm(qkv, q_norm_w, k_norm_w, positions, token_req, Hq, Hkv, block_table, k_cache,
                   v_cache, k_scale, v_scale, q_out, q_scale_out=None, flags=None, *, eps=1e-6,
-                  rope_base=1e6, rope_layout=HPC_ROPE_HALVES, norm_first=True, stream=None):
+                  rope_base=1e6, rope_layout=HPC_ROPE_HALVES, norm_first=True, freq=None,
+                  stream=None):
     """Fused prologue: QK-Norm + RoPE of the new tokens' heads, K/V written into
-    the paged cache, the query into q_out (and q_scale_out for FP8)."""
+    the paged cache, the query into q_out (and q_scale_out for FP8).  `freq`:
+    the table from hpc_rope_frequencies(rope_base), or None."""
     params = hpc_rope_norm_params(float(eps), float(rope_base), int(rope_layout),
-                                  1 if norm_first else 0)
+                                  1 if norm_first else 0,
+                                  None if freq is None else freq.data_ptr())
     _check("hpc_rope_norm", lib().hpc_rope_norm(
         _ptr(qkv), int(qkv.stride(0)), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions),
         _ptr(token_req), int(positions.numel()), int(Hq), int(Hkv), HEAD_DIM, _ptr(block_table),

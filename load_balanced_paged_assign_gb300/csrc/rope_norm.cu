@@ -7,27 +7,33 @@
 // the model's order, writes K and V straight into the paged cache, and emits
 // the FP8 query with its scale for the attention kernel.
 //
-// It is a pure streaming op (about 2.5 KB in and 2 KB out per token at the
-// TP8 Hy3 shape, 20 KB in per token at TP1), so the design is about keeping
-// enough bytes in flight:
-//   * persistent CTAs of 8 warps stride over tokens; a warp owns whole
-//     128-dim head rows (4 dims per lane, 8-byte loads) and issues the loads
-//     of up to 8 of its rows before it processes any;
-//   * the 64 rotation angles of a token are computed once per CTA by two
-//     warps while the loads are in flight: the frequency table base^(-2i/128)
-//     is built once per CTA in fp64, the angle pos * freq is reduced modulo
-//     2 pi in fp64 (a few double operations), and only the reduced angle, in
-//     half turns, goes through fp32 sincospif, so positions in the hundreds
-//     of thousands keep fp32 accuracy;
-//   * the RMS and the FP8 amax are warp reductions, the rotation partner of
-//     a dim is in the same lane (interleaved pairs) or 16 lanes away (halves);
-//   * one __syncthreads per token (the angle table and the token's cache
-//     slot are double-buffered in shared memory).
+// It is a pure streaming op (a token brings (Hq + 2 Hkv) * 256 bytes in and
+// about half of that out), so the design is about bytes in flight and short
+// dependency chains:
+//   * persistent CTAs of 8 warps stride over tokens; each token's fused QKV
+//     row is staged in shared memory by one bulk copy (TMA engine), issued
+//     several tokens ahead through a ring of stages with mbarrier completion
+//     (every wait bounded), so the loads do not hold registers;
+//   * a warp owns the head rows j == warp (mod 8) of each token and runs
+//     same-kind rows (query, key or value) in batches of up to 4, so the
+//     reductions (RMS, FP8 amax) of a batch interleave;
+//   * lanes hold the dims so that every rotated pair sits in one lane (dims
+//     2l, 2l+1, 64+2l, 65+2l for the halves layout; 4l..4l+3 interleaved):
+//     the rotation needs no shuffles;
+//   * RoPE angles come from an fp64 frequency table (given by the caller or
+//     built per CTA); per token the angle pos * freq is formed in fp32 as an
+//     exact product plus its rounding error and reduced modulo 2 pi with a
+//     two-constant split of 2 pi (the Cody-Waite method), so positions up to
+//     2^24 keep an angle error of a few 1e-7 rad;
+//   * the angle table and the token's cache slot for the next token are
+//     computed while the current token is processed (double-buffered), one
+//     __syncthreads per token.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -35,10 +41,22 @@
 namespace hpc {
 namespace {
 
+#ifndef HPC_RN_MIN_CTAS
+#define HPC_RN_MIN_CTAS 3  // resident CTAs per SM the register budget must allow
+#endif
+
 constexpr int kRnWarps = 8;
 constexpr int kRnThreads = 32 * kRnWarps;
-constexpr int kRowsInFlight = 8;  // head rows a warp loads before processing them
-constexpr double kInvPi = 0.3183098861837907;
+constexpr int kMaxStages = 8;
+constexpr int kStageBudget = 40 * 1024;  // QKV bytes a CTA keeps in flight (at least 2 stages)
+constexpr int kRowBytes = kHeadDim * 2;  // one BF16 head row
+constexpr int kMaxPosition = 1 << 24;    // positions are exact in fp32 below this
+constexpr float kTwoPiHi = 6.2831854820251465f;     // fp32(2 pi)
+constexpr float kTwoPiLo = -1.7484555314695172e-7f;  // 2 pi - fp32(2 pi)
+constexpr float kInvTwoPi = 0.159154937f;
+constexpr float kInvPi = 0.318309873f;
+
+enum RowKind { kQ = 0, kK = 1, kV = 2 };
 
 struct RopeNormArgs {
     const uint16_t *qkv;
@@ -48,6 +66,7 @@ struct RopeNormArgs {
     const int32_t *positions;
     const int32_t *token_req;
     const int32_t *block_table;
+    const double *freq;  // [64] or nullptr: built per CTA from base
     void *k_cache;
     void *v_cache;
     void *q_out;
@@ -59,244 +78,471 @@ struct RopeNormArgs {
     float v_scale;
     int N, Hq, Hkv, R;  // R = Hq + 2 Hkv head rows per token
     int B, max_pages, num_pages;
-    int layout;
+    int stages;
     int norm_first;
 };
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+// ------------------------------------------------------------ lane layout
+// A head row is handled by one half-warp (16 lanes, 8 dims each), so a warp
+// instruction covers two rows and a row reduction takes four shuffles.
+// Sub-lane s = lane & 15 holds, and pairs under the rotation:
+//   halves:      dims 4s..4s+3 and 64+4s..67+4s; pairs (x[k], x[4+k])
+//   interleaved: dims 8s..8s+7;                  pairs (x[2k], x[2k+1])
+// In both layouts pair k of sub-lane s has frequency 4s + k.
+
+__device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+    lo = bf16lo_to_f32(w);
+    hi = bf16hi_to_f32(w);
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+template <int LAYOUT>
+__device__ __forceinline__ uint4 load_words(const char *row, int s) {
+    if (LAYOUT == HPC_ROPE_HALVES) {
+        const uint2 lo = *reinterpret_cast<const uint2 *>(row + 8 * s);
+        const uint2 hi = *reinterpret_cast<const uint2 *>(row + 128 + 8 * s);
+        return make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    return *reinterpret_cast<const uint4 *>(row + 16 * s);
 }
 
-// E4M3 (round to nearest even, saturating) of four values -> 4 bytes, v[0] lowest.
-__device__ __forceinline__ uint32_t to_e4m3x4(const float (&v)[4]) {
+template <int LAYOUT>
+__device__ __forceinline__ void store_words(char *row, int s, uint4 v) {
+    if (LAYOUT == HPC_ROPE_HALVES) {
+        *reinterpret_cast<uint2 *>(row + 8 * s) = make_uint2(v.x, v.y);
+        *reinterpret_cast<uint2 *>(row + 128 + 8 * s) = make_uint2(v.z, v.w);
+    } else {
+        *reinterpret_cast<uint4 *>(row + 16 * s) = v;
+    }
+}
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&x)[8]) {
+    unpack2(v.x, x[0], x[1]);
+    unpack2(v.y, x[2], x[3]);
+    unpack2(v.z, x[4], x[5]);
+    unpack2(v.w, x[6], x[7]);
+}
+
+// E4M3 (round to nearest even, saturating) of four values, y[0] in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4(float y0, float y1, float y2, float y3) {
     uint16_t lo, hi;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v[1]), "f"(v[0]));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v[3]), "f"(v[2]));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(y1), "f"(y0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(y3), "f"(y2));
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-__device__ __forceinline__ uint2 to_bf16x4(const float (&v)[4]) {
-    return make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-}
-
-// Rotates this lane's four dims in place; cs holds (cos, sin) per frequency.
-__device__ __forceinline__ void rotate(float (&v)[4], const float2 *cs, int lane, int layout) {
-    if (layout == HPC_ROPE_HALVES) {
-        // dims 4*lane + k; pairs (i, i + 64): lanes 0-15 hold the first
-        // elements, lanes 16-31 the second ones of the same frequencies
-        const bool second = lane >= 16;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[k], 16);
-            const float2 c = cs[(4 * lane + k) & 63];
-            v[k] = second ? fmaf(v[k], c.x, other * c.y) : fmaf(v[k], c.x, -other * c.y);
-        }
+template <int LAYOUT>
+__device__ __forceinline__ void store_e4m3(char *row, int s, const float (&y)[8]) {
+    const uint32_t a = e4m3x4(y[0], y[1], y[2], y[3]), b = e4m3x4(y[4], y[5], y[6], y[7]);
+    if (LAYOUT == HPC_ROPE_HALVES) {
+        *reinterpret_cast<uint32_t *>(row + 4 * s) = a;
+        *reinterpret_cast<uint32_t *>(row + 64 + 4 * s) = b;
     } else {
-        // pairs (2i, 2i + 1): dims 4*lane.. hold frequencies 2*lane and 2*lane + 1
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const float2 c = cs[2 * lane + k];
-            const float a = v[2 * k], b = v[2 * k + 1];
-            v[2 * k] = fmaf(a, c.x, -b * c.y);
-            v[2 * k + 1] = fmaf(b, c.x, a * c.y);
-        }
+        *reinterpret_cast<uint2 *>(row + 8 * s) = make_uint2(a, b);
     }
 }
 
-__device__ __forceinline__ void unpack4(uint2 raw, float (&x)[4]) {
-    x[0] = bf16lo_to_f32(raw.x);
-    x[1] = bf16hi_to_f32(raw.x);
-    x[2] = bf16lo_to_f32(raw.y);
-    x[3] = bf16hi_to_f32(raw.y);
+template <int LAYOUT>
+__device__ __forceinline__ void store_bf16(char *row, int s, const float (&y)[8]) {
+    store_words<LAYOUT>(row, s,
+                        make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                   pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7])));
 }
 
-template <bool FP8>
-__device__ __forceinline__ void process_row(const RopeNormArgs &a, int t, int j, uint2 raw,
-                                            const float2 *cs, long long slot,
-                                            const float (&wq)[4], const float (&wk)[4],
-                                            int lane) {
-    float x[4];
-    unpack4(raw, x);
+// cs = (cos, sin) of this sub-lane's four frequencies, interleaved.
+template <int LAYOUT>
+__device__ __forceinline__ void rotate(float (&x)[8], const float (&cs)[8]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int ia = LAYOUT == HPC_ROPE_HALVES ? k : 2 * k;
+        const int ib = LAYOUT == HPC_ROPE_HALVES ? 4 + k : 2 * k + 1;
+        const float p = x[ia], q = x[ib], c = cs[2 * k], sn = cs[2 * k + 1];
+        x[ia] = fmaf(p, c, -q * sn);
+        x[ib] = fmaf(q, c, p * sn);
+    }
+}
+
+// ------------------------------------------------------------ one batch of rows
+// NP row pairs of one kind.  Pair i of the batch is rows row0 + 16 i and
+// row0 + 16 i + 1; this half-warp takes the one at offset `half`.  Rows at or
+// past `end` (the odd last row of a kind) are computed on a stand-in row and
+// not stored.
+template <bool FP8, int LAYOUT, bool NF, int KIND, int NP>
+__device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *stage, int t,
+                                           int row0, int end, int half, int s,
+                                           const float (&cs)[8], long long slot,
+                                           const float (&w)[8], float kv_scale) {
     constexpr int kElem = FP8 ? 1 : 2;
-    if (j >= a.Hq + a.Hkv) {  // value head: straight into the cache
-        if (slot < 0) return;
-        const int h = j - a.Hq - a.Hkv;
-        char *dst = static_cast<char *>(a.v_cache) +
-                    ((slot * a.Hkv + h) * kHeadDim + 4 * lane) * kElem;
-        if (FP8) {
-            float y[4];
+    if (KIND != kQ && slot < 0) return;  // no cache slot for this token (uniform per CTA)
+    int row[NP];
+    bool valid[NP];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) y[k] = x[k] / a.v_scale;
-            *reinterpret_cast<uint32_t *>(dst) = to_e4m3x4(y);
-        } else {
-            *reinterpret_cast<uint2 *>(dst) = raw;
+    for (int i = 0; i < NP; ++i) {
+        row[i] = row0 + 16 * i + half;
+        valid[i] = row[i] < end;
+        if (!valid[i]) row[i] = end - 1;
+    }
+    if constexpr (KIND == kV && !FP8) {  // BF16 value rows: copied word for word
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const uint4 v = load_words<LAYOUT>(stage + (size_t)row[i] * kRowBytes, s);
+            if (valid[i])
+                store_words<LAYOUT>(static_cast<char *>(a.v_cache) +
+                                        (slot * a.Hkv + (row[i] - a.Hq - a.Hkv)) *
+                                            (kHeadDim * kElem), s, v);
         }
         return;
-    }
-    const bool is_q = j < a.Hq;
-    float w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = is_q ? wq[k] : wk[k];
-    // the rotation keeps the row's norm, so the RMS of x serves both orders
-    const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-    const float inv = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + a.eps);
-    float y[4];
-    if (a.norm_first) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] = x[k] * inv * w[k];
-        rotate(y, cs, lane, a.layout);
     } else {
+        float x[NP][8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] = x[k];
-        rotate(y, cs, lane, a.layout);
+        for (int i = 0; i < NP; ++i)
+            unpack8(load_words<LAYOUT>(stage + (size_t)row[i] * kRowBytes, s), x[i]);
+        if constexpr (KIND == kV) {  // FP8 value rows: true division by the cache scale
+            // (BF16 inputs over the scale often land exactly on an E4M3
+            // midpoint, where only the exact quotient rounds to even)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] = y[k] * inv * w[k];
-    }
-    if (is_q) {
-        const size_t row = (size_t)t * a.Hq + j;
-        if (FP8) {
-            const float amax =
-                warp_max(fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3]))));
-            const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+            for (int i = 0; i < NP; ++i) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) y[k] = y[k] / scale;
-            reinterpret_cast<uint32_t *>(a.q_out)[row * (kHeadDim / 4) + lane] = to_e4m3x4(y);
-            if (lane == 0) a.q_scale_out[row] = scale;
+                for (int k = 0; k < 8; ++k) x[i][k] = __fdiv_rn(x[i][k], kv_scale);
+                if (valid[i])
+                    store_e4m3<LAYOUT>(static_cast<char *>(a.v_cache) +
+                                           (slot * a.Hkv + (row[i] - a.Hq - a.Hkv)) * kHeadDim,
+                                       s, x[i]);
+            }
+            return;
         } else {
-            reinterpret_cast<uint2 *>(a.q_out)[row * (kHeadDim / 4) + lane] = to_bf16x4(y);
-        }
-        return;
-    }
-    if (slot < 0) return;
-    const int h = j - a.Hq;
-    char *dst =
-        static_cast<char *>(a.k_cache) + ((slot * a.Hkv + h) * kHeadDim + 4 * lane) * kElem;
-    if (FP8) {
+            // RMS of the row (the rotation keeps it), then v = the rotated,
+            // weighted row before the norm factor: the output is inv * v
+            float inv[NP];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] = y[k] / a.k_scale;
-        *reinterpret_cast<uint32_t *>(dst) = to_e4m3x4(y);
-    } else {
-        *reinterpret_cast<uint2 *>(dst) = to_bf16x4(y);
-    }
-}
-
-template <bool FP8>
-__global__ void __launch_bounds__(kRnThreads) rope_norm_kernel(const RopeNormArgs a) {
-    __shared__ double s_freq[kHeadDim / 2];
-    __shared__ float2 s_cs[2][kHeadDim / 2];
-    __shared__ long long s_slot[2];  // token's (page * 64 + offset), or -1: no cache write
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    // Everything this grid reads may come from the kernel before it.
-    grid_dependency_wait();
-    if (tid < kHeadDim / 2) s_freq[tid] = pow(a.base, -(double)(2 * tid) / kHeadDim);
-    float wq[4], wk[4];
-    {
-        const uint2 rq = reinterpret_cast<const uint2 *>(a.q_w)[lane];
-        const uint2 rk = reinterpret_cast<const uint2 *>(a.k_w)[lane];
-        unpack4(rq, wq);
-        unpack4(rk, wk);
-    }
-    __syncthreads();
-
-    int it = 0;
-    for (int t = blockIdx.x; t < a.N; t += gridDim.x, ++it) {
-        const int buf = it & 1;
-        const uint2 *row0 = reinterpret_cast<const uint2 *>(a.qkv + (size_t)t * a.stride);
-        uint2 raw[kRowsInFlight];
+            for (int i = 0; i < NP; ++i) {
+                float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < kRowsInFlight; ++k) {
-            const int j = warp + k * kRnWarps;
-            if (j < a.R) raw[k] = __ldcs(row0 + (size_t)j * (kHeadDim / 4) + lane);
-        }
-        if (tid < kHeadDim / 2) {
-            const int pos = a.positions[t];
-            // the angle in half turns, reduced to [-1, 1] exactly in fp64
-            const double turns = (double)pos * s_freq[tid] * kInvPi;
-            const double r = fma(-2.0, rint(0.5 * turns), turns);
-            float sn, c;
-            sincospif((float)r, &sn, &c);
-            s_cs[buf][tid] = make_float2(c, sn);
-        } else if (tid == kHeadDim / 2) {
-            const int pos = a.positions[t];
-            const int req = a.token_req ? a.token_req[t] : t;
-            long long slot = -1;
-            if (req < 0 || req >= a.B || pos < 0 || pos >= a.max_pages * kTile) {
-                if (a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_SEQLEN);
-            } else {
-                const int page = a.block_table[(size_t)req * a.max_pages + pos / kTile];
-                if (page < 0 || page >= a.num_pages) {
-                    if (a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_PAGE);
+                for (int k = 0; k < 8; ++k) ss = fmaf(x[i][k], x[i][k], ss);
+                inv[i] = ss;
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) inv[i] += __shfl_xor_sync(0xffffffffu, inv[i], o);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                inv[i] = rsqrtf(fmaf(inv[i], 1.0f / kHeadDim, a.eps));
+                if constexpr (NF) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[i][k] *= w[k];
+                    rotate<LAYOUT>(x[i], cs);
                 } else {
-                    slot = (long long)page * kTile + (pos % kTile);
+                    rotate<LAYOUT>(x[i], cs);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[i][k] *= w[k];
                 }
             }
-            s_slot[buf] = slot;
+            if constexpr (KIND == kQ) {
+                if (FP8) {
+                    // codes = v * 448 / amax(v): the norm factor cancels; the
+                    // scale is amax(inv * v) / 448
+                    float amax[NP];
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        float m = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(x[i][k]));
+                        amax[i] = m;
+                    }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                        for (int i = 0; i < NP; ++i)
+                            amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xffffffffu, amax[i], o));
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const float ymax = amax[i] * inv[i];
+                        const bool live = ymax > 0.f;
+                        const float mul = live ? __fdividef(448.0f, amax[i]) : 0.f;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) x[i][k] *= mul;
+                        if (valid[i]) {
+                            const size_t qrow = (size_t)t * a.Hq + row[i];
+                            store_e4m3<LAYOUT>(static_cast<char *>(a.q_out) + qrow * kHeadDim, s,
+                                               x[i]);
+                            if (s == 0) a.q_scale_out[qrow] = live ? ymax * (1.0f / 448.0f) : 1.f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) x[i][k] *= inv[i];
+                        if (valid[i])
+                            store_bf16<LAYOUT>(static_cast<char *>(a.q_out) +
+                                                   ((size_t)t * a.Hq + row[i]) * (kHeadDim * 2),
+                                               s, x[i]);
+                    }
+                }
+            } else {  // key rows: into the cache slot
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float m = FP8 ? inv[i] * __frcp_rn(kv_scale) : inv[i];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[i][k] *= m;
+                    if (!valid[i]) continue;
+                    char *dst = static_cast<char *>(a.k_cache) +
+                                (slot * a.Hkv + (row[i] - a.Hq)) * (kHeadDim * kElem);
+                    if (FP8) store_e4m3<LAYOUT>(dst, s, x[i]);
+                    else store_bf16<LAYOUT>(dst, s, x[i]);
+                }
+            }
+        }
+    }
+}
+
+// Rows [begin, end) of one kind form pairs (begin + 2p, begin + 2p + 1); pair
+// p has the global number pair0 + p, and warp w takes the pairs numbered
+// w (mod 8), so consecutive kinds continue the rotation over the warps.
+template <bool FP8, int LAYOUT, bool NF, int KIND>
+__device__ __forceinline__ void rows_of_kind(const RopeNormArgs &a, const char *stage, int t,
+                                             int begin, int end, int pair0, int warp, int half,
+                                             int s, const float (&cs)[8], long long slot,
+                                             const float (&w)[8], float kv_scale) {
+    const int npairs = (end - begin + 1) / 2;
+    int p = ((warp - pair0) % kRnWarps + kRnWarps) % kRnWarps;  // first pair of this warp
+    int count = p < npairs ? (npairs - 1 - p) / kRnWarps + 1 : 0;
+    for (; count >= 2; count -= 2, p += 2 * kRnWarps)
+        rows_batch<FP8, LAYOUT, NF, KIND, 2>(a, stage, t, begin + 2 * p, end, half, s, cs, slot, w,
+                                         kv_scale);
+    if (count) rows_batch<FP8, LAYOUT, NF, KIND, 1>(a, stage, t, begin + 2 * p, end, half, s, cs,
+                                                slot, w, kv_scale);
+}
+
+// cos/sin of pos * freq_i, freq_i = hi + lo (two floats), reduced modulo 2 pi.
+__device__ __forceinline__ float2 rope_angle(int pos, float hi, float lo) {
+    const float p = (float)pos;                 // exact: |pos| < 2^24 for valid tokens
+    const float prod = p * hi;
+    const float err = fmaf(p, hi, -prod);       // exact rounding error of the product
+    const float k = rintf(prod * kInvTwoPi);
+    float r = fmaf(-k, kTwoPiHi, prod);
+    r = fmaf(-k, kTwoPiLo, r);
+    r += fmaf(p, lo, err);                      // the small terms, |.| < 1.5
+    const float k2 = rintf(r * kInvTwoPi);      // back into [-pi, pi]
+    r = fmaf(-k2, kTwoPiHi, r);
+    r = fmaf(-k2, kTwoPiLo, r);
+    float s, c;
+    sincospif(r * kInvPi, &s, &c);
+    return make_float2(c, s);
+}
+
+// The token's cache slot (page * 64 + offset), or -1 with a flag raised.
+__device__ __forceinline__ long long token_slot(const RopeNormArgs &a, int t, int pos, int req) {
+    if (req < 0 || req >= a.B || pos < 0 || pos >= a.max_pages * kTile) {
+        if (a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_SEQLEN);
+        return -1;
+    }
+    const int page = a.block_table[(size_t)req * a.max_pages + pos / kTile];
+    if (page < 0 || page >= a.num_pages) {
+        if (a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_PAGE);
+        return -1;
+    }
+    return (long long)page * kTile + (pos % kTile);
+}
+
+// Bounded wait on an mbarrier phase, uniform across the warp: lane 0 polls,
+// the verdict is broadcast, then every lane observes the phase itself.
+__device__ __forceinline__ bool warp_wait_phase(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
+template <bool FP8, int LAYOUT, bool NF>
+__global__ void __launch_bounds__(kRnThreads, HPC_RN_MIN_CTAS) rope_norm_kernel(const RopeNormArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int row_bytes = a.R * kRowBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * row_bytes);
+    float2 *s_cs = reinterpret_cast<float2 *>(full + kMaxStages);  // [2][64]
+    float *s_fhi = reinterpret_cast<float *>(s_cs + 2 * 64);
+    float *s_flo = s_fhi + 64;
+    long long *s_slot = reinterpret_cast<long long *>(s_flo + 64);  // [2]
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_slot + 2);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grid = gridDim.x;
+    const int n_it = (a.N - (int)blockIdx.x + grid - 1) / grid;  // >= 1: the grid is <= N
+
+    auto issue = [&](int it) {  // bulk copy of iteration it's token row into its stage
+        const int t = blockIdx.x + it * grid;
+        const int s = it % a.stages;
+        mbar_arrive_expect_tx(&full[s], row_bytes);
+        bulk_load(smem + (size_t)s * row_bytes, a.qkv + (size_t)t * a.stride, row_bytes,
+                  &full[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) mbar_init(&full[s], 1);
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    // Everything this grid reads may come from the kernel before it.
+    grid_dependency_wait();
+    int issued = 0;  // (thread 0) iterations whose copy has been issued
+    if (tid == 0)
+        for (; issued < min(a.stages, n_it); ++issued) issue(issued);
+    // the first token's position (and request), in flight with the table below
+    int pos0 = 0, req0 = 0;
+    if (tid <= 64) {
+        pos0 = a.positions[blockIdx.x];
+        req0 = a.token_req ? a.token_req[blockIdx.x] : (int)blockIdx.x;
+    }
+    if (tid < 64) {
+        const double f = a.freq ? a.freq[tid] : pow(a.base, -(double)tid / 64.0);
+        const float hi = (float)f;
+        s_fhi[tid] = hi;
+        s_flo[tid] = (float)(f - (double)hi);
+    }
+    const int half = lane >> 4, sub = lane & 15;
+    float wq[8], wk[8];
+    unpack8(load_words<LAYOUT>(reinterpret_cast<const char *>(a.q_w), sub), wq);
+    unpack8(load_words<LAYOUT>(reinterpret_cast<const char *>(a.k_w), sub), wk);
+    __syncthreads();  // barriers initialised, frequency table ready
+
+    // angles and cache slot of the first token
+    if (tid < 64) s_cs[tid] = rope_angle(pos0, s_fhi[tid], s_flo[tid]);
+    else if (tid == 64) s_slot[0] = token_slot(a, blockIdx.x, pos0, req0);
+
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+        const int t = blockIdx.x + it * grid;
+        const int buf = it & 1;
+        const int stage = it % a.stages;
+        __syncthreads();  // this token's angles and slot are ready; the previous stage is free
+        if (tid == 0 && it >= 1 && it - 1 + a.stages < n_it && !*s_abort)
+            issue(issued++);  // == it - 1 + stages, into the stage freed by iteration it - 1
+        // the next token's position and request, loaded while this one is processed
+        int pos_n = 0, req_n = 0;
+        const bool has_next = it + 1 < n_it;
+        if (tid <= 64 && has_next) {
+            pos_n = a.positions[t + grid];
+            req_n = a.token_req ? a.token_req[t + grid] : t + grid;
+        }
+        if (ok) ok = warp_wait_phase(&full[stage], (uint32_t)(it / a.stages) & 1u, s_abort);
+        if (ok) {
+            const char *st = reinterpret_cast<const char *>(smem) + (size_t)stage * row_bytes;
+            float cs[8];
+            {
+                const float4 *c4 = reinterpret_cast<const float4 *>(s_cs + buf * 64 + 4 * sub);
+                const float4 c0 = c4[0], c1 = c4[1];
+                cs[0] = c0.x, cs[1] = c0.y, cs[2] = c0.z, cs[3] = c0.w;
+                cs[4] = c1.x, cs[5] = c1.y, cs[6] = c1.z, cs[7] = c1.w;
+            }
+            const long long slot = s_slot[buf];
+            const int pq = (a.Hq + 1) / 2, pk = (a.Hkv + 1) / 2;  // pairs of each kind
+            rows_of_kind<FP8, LAYOUT, NF, kQ>(a, st, t, 0, a.Hq, 0, warp, half, sub, cs, slot, wq,
+                                          1.f);
+            rows_of_kind<FP8, LAYOUT, NF, kK>(a, st, t, a.Hq, a.Hq + a.Hkv, pq, warp, half, sub, cs,
+                                          slot, wk, a.k_scale);
+            rows_of_kind<FP8, LAYOUT, NF, kV>(a, st, t, a.Hq + a.Hkv, a.R, pq + pk, warp, half, sub,
+                                          cs, slot, wk, a.v_scale);
+        }
+        if (has_next) {
+            if (tid < 64) s_cs[(buf ^ 1) * 64 + tid] = rope_angle(pos_n, s_fhi[tid], s_flo[tid]);
+            else if (tid == 64) s_slot[buf ^ 1] = token_slot(a, t + grid, pos_n, req_n);
+        }
+    }
+    if (*s_abort) {
+        // a copy never completed: report it, and let no copy land after exit
+        // (a stage holds at most one copy at a time: wait for the last one issued
+        // into each stage, again with a time limit)
+        if (tid == 0) {
+            if (a.flags) atomicOr(a.flags, (int)HPC_FLAG_TIMEOUT);
+            for (int it = max(0, issued - a.stages); it < issued; ++it) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&full[it % a.stages], (uint32_t)(it / a.stages) & 1u) &&
+                       globaltimer_ns() - t0 < 1000000000ull) {
+                }
+            }
         }
         __syncthreads();
-        const float2 *cs = s_cs[buf];
-        const long long slot = s_slot[buf];
-        for (int base = warp;;) {
-#pragma unroll
-            for (int k = 0; k < kRowsInFlight; ++k) {
-                const int j = base + k * kRnWarps;
-                if (j < a.R) process_row<FP8>(a, t, j, raw[k], cs, slot, wq, wk, lane);
-            }
-            base += kRowsInFlight * kRnWarps;
-            if (base >= a.R) break;
-#pragma unroll
-            for (int k = 0; k < kRowsInFlight; ++k) {
-                const int j = base + k * kRnWarps;
-                if (j < a.R) raw[k] = __ldcs(row0 + (size_t)j * (kHeadDim / 4) + lane);
-            }
-        }
     }
 }
 
+__global__ void rope_frequencies_kernel(double base, double *freq) {
+    const int i = threadIdx.x;
+    if (i < kHeadDim / 2) freq[i] = pow(base, -(double)(2 * i) / kHeadDim);
+}
+
+// ------------------------------------------------------------ host side
+using KernelFn = void (*)(const RopeNormArgs);
+
+template <bool FP8, int LAYOUT>
+KernelFn kernel_for_order(bool norm_first) {
+    return norm_first ? rope_norm_kernel<FP8, LAYOUT, true> : rope_norm_kernel<FP8, LAYOUT, false>;
+}
+
+KernelFn kernel_for(bool fp8, int layout, bool norm_first) {
+    if (fp8) return layout == HPC_ROPE_HALVES
+                        ? kernel_for_order<true, HPC_ROPE_HALVES>(norm_first)
+                        : kernel_for_order<true, HPC_ROPE_INTERLEAVED>(norm_first);
+    return layout == HPC_ROPE_HALVES ? kernel_for_order<false, HPC_ROPE_HALVES>(norm_first)
+                                     : kernel_for_order<false, HPC_ROPE_INTERLEAVED>(norm_first);
+}
+
+size_t smem_bytes(int R, int stages) {
+    return (size_t)stages * R * kRowBytes + kMaxStages * 8 + 2 * 64 * 8 + 2 * 64 * 4 + 2 * 8 + 16;
+}
+
+// Per device and kernel variant: the dynamic shared memory already allowed,
+// and the last occupancy query (for one shared-memory size).
+struct VariantCache {
+    int smem_allowed = 0;
+    int smem_queried = -1;
+    int cap = 0;
+};
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_grid_cap[kMaxDevices][2];  // resident CTAs per device and dtype (0: unknown)
+VariantCache g_cache[kMaxDevices][8];
+std::mutex g_cache_mutex;
 
-template <bool FP8>
-int grid_cap() {
+cudaError_t launch(const RopeNormArgs &a, bool fp8, int layout, cudaStream_t s) {
+    const bool nf = a.norm_first != 0;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < kMaxDevices) {
-        const int c = g_grid_cap[dev][FP8].load();
-        if (c > 0) return c;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const KernelFn fn = kernel_for(fp8, layout, nf);
+    const int smem = (int)smem_bytes(a.R, a.stages);
+    int cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        VariantCache &vc = g_cache[dev][(fp8 ? 4 : 0) + 2 * layout + (nf ? 1 : 0)];
+        if (smem > vc.smem_allowed) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            vc.smem_allowed = smem;
+        }
+        if (vc.smem_queried != smem) {
+            int sms = 0, per_sm = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRnThreads, smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) return cudaErrorInvalidConfiguration;
+            vc.smem_queried = smem;
+            vc.cap = sms * per_sm;
+        }
+        cap = vc.cap;
     }
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope_norm_kernel<FP8>, kRnThreads,
-                                                      0) != cudaSuccess ||
-        per_sm < 1)
-        return 0;
-    const int cap = sms * per_sm;
-    if (dev >= 0 && dev < kMaxDevices) g_grid_cap[dev][FP8].store(cap);
-    return cap;
-}
-
-template <bool FP8>
-cudaError_t launch(const RopeNormArgs &a, cudaStream_t s) {
-    const int cap = grid_cap<FP8>();
-    if (cap < 1) return cudaErrorUnknown;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(a.N, cap));
     cfg.blockDim = dim3(kRnThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rope_norm_kernel<FP8>, a);
+    return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -305,6 +551,14 @@ bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
 
 }  // namespace
 }  // namespace hpc
+
+extern "C" hpc_status hpc_rope_frequencies(float rope_base, double *d_freq, hpc_stream_t stream) {
+    using namespace hpc;
+    if (!finite_positive(rope_base) || !d_freq || !aligned16(d_freq)) return HPC_ERR_ARG;
+    rope_frequencies_kernel<<<1, kHeadDim / 2, 0, static_cast<cudaStream_t>(stream)>>>(
+        (double)rope_base, d_freq);
+    return cudaGetLastError() == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
 
 extern "C" hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride,
                                     const void *d_q_norm_w, const void *d_k_norm_w,
@@ -321,7 +575,9 @@ extern "C" hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride,
         num_pages <= 0)
         return HPC_ERR_ARG;
     if (head_dim != HPC_HEAD_DIM || Hq % Hkv != 0) return HPC_ERR_UNSUPPORTED;
-    if (Hq + 2 * Hkv > 4096) return HPC_ERR_UNSUPPORTED;
+    const int R = Hq + 2 * Hkv;
+    int stages = std::min(kMaxStages, std::max(2, kStageBudget / (R * kRowBytes)));
+    if (smem_bytes(R, stages) > 200 * 1024) return HPC_ERR_UNSUPPORTED;  // > ~390 head rows
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
     if (!std::isfinite(params->eps) || params->eps < 0.f || !finite_positive(params->rope_base))
@@ -329,15 +585,16 @@ extern "C" hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride,
     if (params->rope_layout != HPC_ROPE_HALVES && params->rope_layout != HPC_ROPE_INTERLEAVED)
         return HPC_ERR_ARG;
     if (params->norm_first != 0 && params->norm_first != 1) return HPC_ERR_ARG;
+    if (params->freq && !aligned16(params->freq)) return HPC_ERR_ARG;
     if (fp8 && (!finite_positive(k_scale) || !finite_positive(v_scale))) return HPC_ERR_ARG;
     if ((int64_t)B * max_pages_per_req >= (int64_t)1 << 31) return HPC_ERR_UNSUPPORTED;
-    if ((int64_t)max_pages_per_req * kTile >= (int64_t)1 << 31) return HPC_ERR_UNSUPPORTED;
+    // cache positions must stay exact in fp32 (the RoPE angle is formed there)
+    if ((int64_t)max_pages_per_req * kTile > kMaxPosition) return HPC_ERR_UNSUPPORTED;
     if (num_tokens == 0) return HPC_OK;
     if (!d_qkv || !d_q_norm_w || !d_k_norm_w || !d_positions || !d_block_table || !d_k_cache ||
         !d_v_cache || !d_q_out || (fp8 && !d_q_scale_out))
         return HPC_ERR_ARG;
-    if (qkv_row_stride < (int64_t)(Hq + 2 * Hkv) * HPC_HEAD_DIM || qkv_row_stride % 8 != 0)
-        return HPC_ERR_ARG;
+    if (qkv_row_stride < (int64_t)R * HPC_HEAD_DIM || qkv_row_stride % 8 != 0) return HPC_ERR_ARG;
     if (!aligned16(d_qkv) || !aligned16(d_q_norm_w) || !aligned16(d_k_norm_w) ||
         !aligned16(d_k_cache) || !aligned16(d_v_cache) || !aligned16(d_q_out))
         return HPC_ERR_ARG;
@@ -351,6 +608,7 @@ extern "C" hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride,
     a.positions = d_positions;
     a.token_req = d_token_req;
     a.block_table = d_block_table;
+    a.freq = params->freq;
     a.k_cache = d_k_cache;
     a.v_cache = d_v_cache;
     a.q_out = d_q_out;
@@ -363,13 +621,12 @@ extern "C" hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride,
     a.N = num_tokens;
     a.Hq = Hq;
     a.Hkv = Hkv;
-    a.R = Hq + 2 * Hkv;
+    a.R = R;
     a.B = B;
     a.max_pages = max_pages_per_req;
     a.num_pages = num_pages;
-    a.layout = params->rope_layout;
+    a.stages = stages;
     a.norm_first = params->norm_first;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 ? launch<true>(a, s) : launch<false>(a, s);
+    const cudaError_t e = launch(a, fp8, params->rope_layout, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }

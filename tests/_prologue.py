@@ -61,6 +61,9 @@ def run_oracle(inp, k_cache0, v_cache0, tokens=None, **overrides):
         req = np.asarray(tokens) if req is None else req[tokens]
     p = dict(eps=w.eps, base=w.rope_base, style=w.rope_layout, norm_first=w.norm_first)
     p.update(overrides)
+    # the C ABI takes eps and the base as fp32: the oracle uses the same values
+    p["eps"] = float(np.float32(p["eps"]))
+    p["base"] = float(np.float32(p["base"]))
     return rn.rope_norm(qkv, words(inp.q_norm_w), words(inp.k_norm_w), pos, req, w.num_q_heads,
                         w.num_kv_heads, inp.block_table.cpu().numpy(), k_cache0, v_cache0,
                         w.kv_dtype, inp.k_scale, inp.v_scale, p["eps"], p["base"], p["style"],

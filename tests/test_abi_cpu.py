@@ -147,12 +147,13 @@ def test_fused_attention_argument_checks(hd):
 
 
 def call_rope_norm(hd, qkv=FAKE, stride=1280, N=4, Hq=8, Hkv=1, D=128, B=4, dtype=0,
-                   q_scale=None, qout=FAKE, params="default", token_req=None, k_scale=1.0):
+                   q_scale=None, qout=FAKE, params="default", token_req=None, k_scale=1.0,
+                   max_pages=16):
     P = hd.binding.hpc_rope_norm_params
-    p = P(1e-6, 1e6, 0, 1) if params == "default" else params
+    p = P(1e-6, 1e6, 0, 1, None) if params == "default" else params
     return hd.lib().hpc_rope_norm(qkv, stride, FAKE, FAKE, FAKE, token_req, N, Hq, Hkv, D, FAKE,
-                                  16, B, FAKE, FAKE, 10, dtype, k_scale, 1.0, qout, q_scale, None,
-                                  None if p is None else ctypes.byref(p), None)
+                                  max_pages, B, FAKE, FAKE, 10, dtype, k_scale, 1.0, qout,
+                                  q_scale, None, None if p is None else ctypes.byref(p), None)
 
 
 def test_rope_norm_argument_checks(hd):
@@ -170,8 +171,16 @@ def test_rope_norm_argument_checks(hd):
     assert call_rope_norm(hd, dtype=5) == E.HPC_ERR_ARG
     assert call_rope_norm(hd, N=5, B=4) == E.HPC_ERR_ARG  # token t is request t: needs N <= B
     assert call_rope_norm(hd, qout=None) == E.HPC_ERR_ARG
-    assert call_rope_norm(hd, params=P(-1.0, 1e6, 0, 1)) == E.HPC_ERR_ARG
-    assert call_rope_norm(hd, params=P(1e-6, 0.0, 0, 1)) == E.HPC_ERR_ARG
-    assert call_rope_norm(hd, params=P(1e-6, float("inf"), 0, 1)) == E.HPC_ERR_ARG
-    assert call_rope_norm(hd, params=P(1e-6, 1e6, 2, 1)) == E.HPC_ERR_ARG
-    assert call_rope_norm(hd, params=P(1e-6, 1e6, 0, 2)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(-1.0, 1e6, 0, 1, None)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 0.0, 0, 1, None)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, float("inf"), 0, 1, None)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 1e6, 2, 1, None)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 1e6, 0, 2, None)) == E.HPC_ERR_ARG
+    assert call_rope_norm(hd, params=P(1e-6, 1e6, 0, 1, FAKE + 8)) == E.HPC_ERR_ARG  # freq
+    # positions must stay exact in fp32: at most 2^24 cache slots per request
+    assert call_rope_norm(hd, max_pages=(1 << 18) + 1) == E.HPC_ERR_UNSUPPORTED
+    assert call_rope_norm(hd, Hq=400, Hkv=8) == E.HPC_ERR_UNSUPPORTED  # too many head rows
+    L = hd.lib()
+    assert L.hpc_rope_frequencies(0.0, FAKE, None) == E.HPC_ERR_ARG
+    assert L.hpc_rope_frequencies(1e4, None, None) == E.HPC_ERR_ARG
+    assert L.hpc_rope_frequencies(1e4, FAKE + 8, None) == E.HPC_ERR_ARG

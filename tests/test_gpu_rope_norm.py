@@ -11,6 +11,7 @@ import torch
 
 import load_balanced_paged_assign_gb300 as hd
 import oracle
+from oracle import rope_norm as rn
 from _gpu import TOL, assert_close, run_step
 from _prologue import check_against_oracle, run_gpu, words
 from load_balanced_paged_assign_gb300.workloads import (PROLOGUES, PrologueInputs,
@@ -22,6 +23,12 @@ pytestmark = pytest.mark.gpu
 
 def snapshot(inp):
     return words(inp.k_cache).copy(), words(inp.v_cache).copy()
+
+
+def freq_table(base):
+    f = torch.empty(64, dtype=torch.float64, device="cuda")
+    hd.hpc_rope_frequencies(base, f)
+    return f
 
 
 def run_and_check(inp, tokens=None, **overrides):
@@ -36,7 +43,14 @@ def run_and_check(inp, tokens=None, **overrides):
     return q, qs, flags, res
 
 
-SHAPES = [(8, 1), (4, 2), (64, 8), (2, 2)]
+def test_frequency_table_matches_the_oracle():
+    for base in (10000.0, 1e6, 500000.0, 2.5):
+        got = freq_table(base).cpu().numpy()
+        ref = rn.rope_frequencies(128, float(np.float32(base)))
+        assert np.allclose(got, ref, rtol=1e-15, atol=0)
+
+
+SHAPES = [(8, 1), (4, 2), (64, 8), (2, 2), (16, 16)]
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
@@ -48,14 +62,25 @@ def test_prefill_shapes(kv_dtype, layout, norm_first, shape):
     pw = PrologueWorkload(f"p{shape}", Hq, Hkv, kv_dtype=kv_dtype, prefill_tokens=150 + shape,
                           rope_layout=layout, norm_first=norm_first, rope_base=10000.0,
                           seed=40 + shape)
-    run_and_check(make_prologue_inputs(pw, device="cuda"))
+    # every other case takes the caller's frequency table
+    table = {"freq": freq_table(10000.0)} if (shape + layout) % 2 else {}
+    run_and_check(make_prologue_inputs(pw, device="cuda"), **table)
 
 
 @pytest.mark.parametrize("name", ["decode_hy3_tp8", "decode_fp8"])
-def test_decode_workloads(name):
-    inp = make_prologue_inputs(PROLOGUES[name], device="cuda")
-    _, _, flags, res = run_and_check(inp)
+@pytest.mark.parametrize("table", [False, True])
+def test_decode_workloads(name, table):
+    pw = PROLOGUES[name]
+    inp = make_prologue_inputs(pw, device="cuda")
+    _, _, flags, res = run_and_check(inp, **({"freq": freq_table(pw.rope_base)} if table else {}))
     assert flags == 0 and all(s is not None for s in res.slots)
+
+
+def test_more_tokens_than_resident_ctas():
+    """Many tokens per CTA: the staging ring wraps many times."""
+    pw = PrologueWorkload("wrap", 8, 1, kv_dtype="e4m3", prefill_tokens=20000, seed=47)
+    inp = make_prologue_inputs(pw, device="cuda")
+    run_and_check(inp, tokens=list(range(0, 20000, 97)) + [19999], freq=freq_table(1e6))
 
 
 @pytest.mark.parametrize("name", ["prefill_8k_fp8", "prefill_8k_bf16"])
@@ -74,7 +99,8 @@ def test_full_size_prefill_sampled(name):
 
 
 def test_long_positions_keep_their_angles():
-    """Positions up to 2^20 with a small base: the fp64 angle reduction must hold."""
+    """Positions up to 2^20 with a small base: the extended-precision angle
+    reduction must hold."""
     N, Hq, Hkv = 48, 4, 1
     rng = np.random.default_rng(11)
     pos = np.sort(rng.choice(1 << 20, N, replace=False)).astype(np.int32)
