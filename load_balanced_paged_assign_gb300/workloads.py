@@ -17,7 +17,9 @@ Recipe (draw order: seqlens, page permutation, Q, K, V):
   * pages: P = sum_r ceil(L_r / 64) physical pages; a random permutation of
     [0, P) is handed out to the requests in request order; unused
     block-table entries are -1;
-  * Q ~ N(0, 1) from the same CPU generator;
+  * Q ~ N(0, 1) from the same CPU generator, [B, Hq, 128], or
+    [B, q_len, Hq, 128] for multi-query decode (q_len > 1: the request's
+    last q_len live tokens are the queries);
   * K, V ~ N(0, 1), drawn on the target device from a generator seeded with
     seed + 1 (K) and seed + 2 (V); slots past L_r in a request's last page
     are part of the draw, or are poisoned (NaN / the E4M3 NaN code) on request;
@@ -53,6 +55,7 @@ class Workload:
     num_ctas: int = 0  # 0: one persistent CTA per resident slot on the GPU
     min_tiles: int = 2
     description: str = ""
+    q_len: int = 1  # query tokens per request (> 1: speculative / MTP decode)
 
     @property
     def group(self) -> int:
@@ -124,10 +127,10 @@ class Batch:
     workload: Workload
     seqlens: torch.Tensor  # int32 [B]
     block_table: torch.Tensor  # int32 [B, max_pages], -1 past each request's pages
-    q: torch.Tensor  # bf16 or float8_e4m3fn [B, Hq, 128]
+    q: torch.Tensor  # bf16 or float8_e4m3fn [B, Hq, 128] ([B, q_len, Hq, 128] for q_len > 1)
     k_cache: torch.Tensor  # bf16 or float8_e4m3fn [P, 64, Hkv, 128]
     v_cache: torch.Tensor
-    q_scale: torch.Tensor | None = None  # fp32 [B, Hq] (FP8 only)
+    q_scale: torch.Tensor | None = None  # fp32 [B, Hq] ([B, q_len, Hq] for q_len > 1; FP8 only)
     k_scale: float = 1.0
     v_scale: float = 1.0
     extras: dict = field(default_factory=dict)
@@ -174,7 +177,8 @@ def make_batch(w: Workload, device="cpu", seed: int | None = None, poison_tail: 
         bt[r, :n] = perm[off:off + n].to(torch.int32)
         off += n
     Hq, Hkv = w.num_q_heads, w.num_kv_heads
-    q32 = torch.randn((B, Hq, HEAD_DIM), generator=gen, dtype=torch.float32)
+    q_shape = (B, Hq, HEAD_DIM) if w.q_len == 1 else (B, w.q_len, Hq, HEAD_DIM)
+    q32 = torch.randn(q_shape, generator=gen, dtype=torch.float32)
     kv_shape = (max(total_pages, 1), PAGE, Hkv, HEAD_DIM)
     k32 = _normal(kv_shape, seed + 1, device)
     v32 = _normal(kv_shape, seed + 2, device)

@@ -24,7 +24,7 @@ from .assign import (TaskMap, assign_closed_form, assign_simulate, budget_of, st
 __all__ = [
     "TaskMap", "assign_closed_form", "assign_simulate", "budget_of", "static_plan", "tiles_of",
     "build", "bf16_to_double", "e4m3_to_double", "attention", "partial", "combine",
-    "split_attention", "BF16", "E4M3",
+    "split_attention", "attention_mq", "BF16", "E4M3",
 ]
 
 BF16 = 0
@@ -64,6 +64,8 @@ def _load():
     lib.oracle_attention.argtypes = common + [dp, i64, dp, i32]
     lib.oracle_partial.restype = i32
     lib.oracle_partial.argtypes = common + [i32, i32, i32, i32, dp, dp]
+    lib.oracle_attention_mq.restype = i32
+    lib.oracle_attention_mq.argtypes = common + [i32, dp, i64, dp, i32]
     lib.oracle_combine.restype = None
     lib.oracle_combine.argtypes = [dp, dp, i32, i32, dp]
     _lib = lib
@@ -152,6 +154,38 @@ def attention(q, k_cache, v_cache, block_table, seqlens, *, rows=None, num_threa
     rc = _load().oracle_attention(*p.head(), _ptr(rows_arr), n, _ptr(out), int(num_threads))
     if rc != 0:
         raise MemoryError("oracle_attention: scratch allocation failed")
+    return out
+
+
+def attention_mq(q, k_cache, v_cache, block_table, seqlens, q_len, *, rows=None, num_threads=0,
+                 **kw):
+    """Multi-query decode attention: q [B, q_len, Hq, D] (q_scale [B, q_len, Hq]
+    for FP8), query token i of request r sees live tokens j < L_r - q_len + 1 + i.
+
+    Returns float64 [B, q_len, Hq, D], or [len(rows), D] for flat rows
+    (r * q_len + i) * Hq + hq."""
+    q_len = int(q_len)
+    qs = kw.get("q_scale")
+    B = int(_i32(seqlens).shape[0])
+    Hq = kw["num_q_heads"]
+    # the query rows are handed over as B * q_len "requests" of Hq heads
+    q2 = q.reshape(B * q_len, Hq, -1) if hasattr(q, "reshape") else q
+    kw2 = dict(kw)
+    if qs is not None:
+        kw2["q_scale"] = qs.reshape(B * q_len, Hq)
+    p = _Problem(q2, k_cache, v_cache, block_table, seqlens, **kw2)
+    p.B = B
+    if rows is None:
+        out = np.zeros((B, q_len, p.Hq, p.D), dtype=np.float64)
+        rows_arr, n = None, B * q_len * p.Hq
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = int(rows_arr.size)
+        out = np.zeros((n, p.D), dtype=np.float64)
+    rc = _load().oracle_attention_mq(*p.head(), q_len, _ptr(rows_arr), n, _ptr(out),
+                                     int(num_threads))
+    if rc != 0:
+        raise MemoryError("oracle_attention_mq: scratch allocation failed")
     return out
 
 

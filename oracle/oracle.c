@@ -28,6 +28,12 @@
  *  - oracle_combine: merge of partials under the global softmax
  *    normalisation (SGLang post, execution paragraph of the live-KV
  *    scheduling section; vLLM post, "Compute and combine").
+ *  - oracle_attention_mq: decode with q_len new query tokens per request
+ *    (the speculative / MTP layer of Hy3, vLLM post "A Quick Word on
+ *    Hy3-series models"): the request's last q_len live tokens are the
+ *    queries, q is [B, q_len, Hq, D], and query token i sees the live tokens
+ *    j < L_r - q_len + 1 + i (everything before it and itself), the plain
+ *    causal reading.  Query rows with no visible token yield zero rows.
  *
  * Inputs are raw storage words: bf16 as uint16 bit patterns, FP8-E4M3 as
  * bytes.  Both are decoded here from their bit-level format definitions
@@ -88,14 +94,15 @@ typedef struct {
     const int32_t *seqlens; /* [B] */
     int B, Hq, Hkv, D, page;
     double sm_scale;
+    int q_len; /* query tokens per request (1: plain decode) */
 } oracle_problem;
 
-/* Dequantised q[r, hq, :] into qv[D]. */
-static void load_query(const oracle_problem *p, int r, int hq, double *qv) {
-    size_t base = ((size_t)r * p->Hq + hq) * p->D;
+/* Dequantised query qi = i * Hq + hq of request r (q is [B, q_len, Hq, D]) into qv[D]. */
+static void load_query(const oracle_problem *p, int r, int qi, double *qv) {
+    size_t row = (size_t)r * p->q_len * p->Hq + qi;
     double scale = 1.0;
-    if (p->q_dtype == ORACLE_E4M3) scale = (double)p->q_scale[(size_t)r * p->Hq + hq];
-    for (int d = 0; d < p->D; ++d) qv[d] = load_elem(p->q, p->q_dtype, base + d) * scale;
+    if (p->q_dtype == ORACLE_E4M3) scale = (double)p->q_scale[row];
+    for (int d = 0; d < p->D; ++d) qv[d] = load_elem(p->q, p->q_dtype, row * p->D + d) * scale;
 }
 
 /* Offset of k[r, j, h, 0] inside a cache, through the block table. */
@@ -106,18 +113,18 @@ static size_t kv_offset(const oracle_problem *p, int r, int j, int h) {
 }
 
 /*
- * Attention of query (r, hq) over live tokens [j0, j1).  Writes the
- * normalised output o[D] and returns the natural-log log-sum-exp of the
- * scaled scores; an empty range gives o = 0 and returns -INFINITY.
- * s and qv are caller scratch of sizes (j1 - j0) and D.
+ * Attention of query qi = i * Hq + hq of request r over live tokens
+ * [j0, j1).  Writes the normalised output o[D] and returns the natural-log
+ * log-sum-exp of the scaled scores; an empty range gives o = 0 and returns
+ * -INFINITY.  s and qv are caller scratch of sizes (j1 - j0) and D.
  */
-static double attend_range(const oracle_problem *p, int r, int hq, int j0, int j1, double *o,
+static double attend_range(const oracle_problem *p, int r, int qi, int j0, int j1, double *o,
                            double *s, double *qv) {
     int G = p->Hq / p->Hkv;
-    int h = hq / G;
+    int h = (qi % p->Hq) / G;
     for (int d = 0; d < p->D; ++d) o[d] = 0.0;
     if (j1 <= j0) return -INFINITY;
-    load_query(p, r, hq, qv);
+    load_query(p, r, qi, qv);
     double kscale = p->kv_dtype == ORACLE_E4M3 ? p->k_scale : 1.0;
     double vscale = p->kv_dtype == ORACLE_E4M3 ? p->v_scale : 1.0;
     double smax = -INFINITY;
@@ -157,7 +164,7 @@ int oracle_attention(const void *q, int q_dtype, const float *q_scale, const voi
                      int Hkv, int D, int page, double sm_scale, const int64_t *rows, int64_t n_rows,
                      double *out, int num_threads) {
     oracle_problem p = {q, q_dtype, q_scale, k_cache, v_cache, kv_dtype, k_scale, v_scale,
-                        block_table, max_pages, seqlens, B, Hq, Hkv, D, page, sm_scale};
+                        block_table, max_pages, seqlens, B, Hq, Hkv, D, page, sm_scale, 1};
     int64_t total = rows ? n_rows : (int64_t)B * Hq;
     int lmax = max_seqlen(&p);
     int failed = 0;
@@ -196,7 +203,7 @@ int oracle_partial(const void *q, int q_dtype, const float *q_scale, const void 
                    int Hkv, int D, int page, double sm_scale, int r, int hq, int j0, int j1, double *o,
                    double *lse) {
     oracle_problem p = {q, q_dtype, q_scale, k_cache, v_cache, kv_dtype, k_scale, v_scale,
-                        block_table, max_pages, seqlens, B, Hq, Hkv, D, page, sm_scale};
+                        block_table, max_pages, seqlens, B, Hq, Hkv, D, page, sm_scale, 1};
     int n = j1 > j0 ? j1 - j0 : 1;
     double *s = (double *)malloc(sizeof(double) * (size_t)n);
     double *qv = (double *)malloc(sizeof(double) * (size_t)D);
@@ -209,6 +216,50 @@ int oracle_partial(const void *q, int q_dtype, const float *q_scale, const void 
     free(s);
     free(qv);
     return 0;
+}
+
+/*
+ * Multi-query decode attention for the listed rows (row = (r * q_len + i) *
+ * Hq + hq; rows == NULL means every row in order).  Query token i of
+ * request r attends live tokens [0, L_r - q_len + 1 + i).  out is
+ * [n_rows, D] fp64.  Returns 0, or -1 when a scratch allocation fails.
+ */
+int oracle_attention_mq(const void *q, int q_dtype, const float *q_scale, const void *k_cache,
+                        const void *v_cache, int kv_dtype, double k_scale, double v_scale,
+                        const int32_t *block_table, int max_pages, const int32_t *seqlens, int B,
+                        int Hq, int Hkv, int D, int page, double sm_scale, int q_len,
+                        const int64_t *rows, int64_t n_rows, double *out, int num_threads) {
+    oracle_problem p = {q, q_dtype, q_scale, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                        block_table, max_pages, seqlens, B, Hq, Hkv, D, page, sm_scale, q_len};
+    int64_t per_req = (int64_t)q_len * Hq;
+    int64_t total = rows ? n_rows : (int64_t)B * per_req;
+    int lmax = max_seqlen(&p);
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+#pragma omp parallel reduction(| : failed)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(lmax > 0 ? lmax : 1));
+        double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!s || !qv) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t n = 0; n < total; ++n) {
+                int64_t row = rows ? rows[n] : n;
+                int r = (int)(row / per_req), qi = (int)(row % per_req);
+                int i = qi / Hq;
+                int visible = seqlens[r] - q_len + 1 + i;
+                attend_range(&p, r, qi, 0, visible, out + n * D, s, qv);
+            }
+        }
+        free(s);
+        free(qv);
+    }
+    return failed ? -1 : 0;
 }
 
 /*

@@ -206,3 +206,81 @@ def test_sampled_rows_match_full():
     got = run_oracle(batch, rows=rows)
     for i, row in enumerate(rows):
         assert np.array_equal(got[i], full.reshape(-1, 128)[row])
+
+
+# ------------------------------------------------------- multi-query decode
+# q_len new query tokens per request (the last q_len live tokens); query
+# token i sees the live tokens j < L - q_len + 1 + i.
+
+def mq_batch(kv_dtype, q_len, lens, hq=8, hkv=2, seed=21):
+    w = Workload("mq", len(lens), hq, hkv, seqlens=tuple(lens), kv_dtype=kv_dtype, seed=seed,
+                 q_len=q_len)
+    return make_batch(w, poison_tail=True)
+
+
+def run_mq(batch, **extra):
+    return oracle.attention_mq(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                               batch.seqlens, batch.workload.q_len, **batch.oracle_kwargs(),
+                               **extra)
+
+
+def sdpa_causal_reference(batch):
+    """torch SDPA (fp64) with an explicit mask: query i sees keys j <= L - q_len + i."""
+    w = batch.workload
+    G, ql = w.group, w.q_len
+    fp8 = w.kv_dtype == "e4m3"
+    q = dequant(batch.q, batch.q_scale.to(torch.float64)[..., None] if fp8 else None)
+    k_all = dequant(batch.k_cache, batch.k_scale if fp8 else None)
+    v_all = dequant(batch.v_cache, batch.v_scale if fp8 else None)
+    out = np.zeros((len(batch.seqlens), ql, w.num_q_heads, 128))
+    for r, L in enumerate(batch.seqlens.tolist()):
+        idx = torch.arange(L)
+        pages = batch.block_table[r].long()[idx // 64]
+        k = k_all[pages, idx % 64].repeat_interleave(G, dim=1).transpose(0, 1)  # [Hq, L, D]
+        v = v_all[pages, idx % 64].repeat_interleave(G, dim=1).transpose(0, 1)
+        mask = idx[None, :] <= (L - ql + torch.arange(ql))[:, None]  # [q_len, L]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[r].transpose(0, 1), k, v, attn_mask=mask, scale=w.sm_scale)  # [Hq, q_len, D]
+        out[r] = o.transpose(0, 1).numpy()
+    return out
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("q_len,hq,hkv", [(2, 8, 2), (3, 4, 4), (4, 4, 1), (2, 16, 2)])
+def test_multi_query_matches_library_sdpa_with_causal_mask(kv_dtype, q_len, hq, hkv):
+    lens = [q_len, 63 + q_len, 64, 65, 129, 200]
+    batch = mq_batch(kv_dtype, q_len, lens, hq, hkv)
+    got = run_mq(batch)
+    ref = sdpa_causal_reference(batch)
+    assert np.allclose(got, ref, atol=1e-12, rtol=1e-10)
+
+
+def test_multi_query_single_token_is_plain_decode():
+    w = Workload("mq1", 5, 8, 2, seqlens=(1, 64, 65, 300, 1000), seed=23)
+    batch = make_batch(w)
+    got = oracle.attention_mq(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                              batch.seqlens, 1, **batch.oracle_kwargs())
+    assert np.array_equal(got[:, 0], run_oracle(batch))
+
+
+def test_multi_query_closed_forms():
+    # the first query of a request of exactly q_len tokens sees only token 0:
+    # its output is v_0 of its KV head; the last query sees every token
+    q_len = 3
+    batch = mq_batch("bf16", q_len, [q_len, 70], hq=4, hkv=2)
+    out = run_mq(batch)
+    v = batch.v_cache.to(torch.float64)
+    p0 = int(batch.block_table[0, 0])
+    for hq in range(4):
+        assert np.array_equal(out[0, 0, hq], v[p0, 0, hq // 2].numpy())
+    # a request shorter than q_len: queries with no visible token give zeros
+    short = mq_batch("bf16", 4, [2, 5], hq=4, hkv=1)
+    out = run_mq(short)
+    assert not out[0, :2].any() and out[0, 2:].any()
+
+
+def test_multi_query_rows_match_full():
+    batch = mq_batch("e4m3", 2, [64, 130, 7], hq=8, hkv=1)
+    full = run_mq(batch).reshape(-1, 128)
+    rows = [0, 5, 17, 31, 47]
+    assert np.array_equal(run_mq(batch, rows=rows), full[rows])
