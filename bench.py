@@ -37,12 +37,13 @@ METRIC = "decode-attn µs/step and achieved HBM GB/s (% of GB300 peak) on mixed-
 
 
 # ------------------------------------------------------------------ byte model
-def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc, split_desc):
+def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc, split_desc, q_len=1):
     """Bytes each kernel must move at minimum.
 
     KV: every live token's K and V row of every KV head once,
-      sum_r L_r * Hkv * 128 * 2 * bpe;  Q: B * Hq * 128 * bpe (+ fp32 q-scales
-      for FP8);  out: B * Hq * 128 * 2;  a partial: G * (128 + 1) * 4.
+      sum_r L_r * Hkv * 128 * 2 * bpe;  Q: B * q_len * Hq * 128 * bpe (+ fp32
+      q-scales for FP8);  out: B * q_len * Hq * 128 * 2;  a partial:
+      q_len * G * (128 + 1) * 4 (q_len query tokens per request, 1 for decode).
     attn (separate combine): KV + Q + one partial written per descriptor.
     combine: those partials read + out.
     attn_fused (the launch the roofline uses): KV + Q + out + the partials of
@@ -53,11 +54,11 @@ def algorithmic_bytes(seqlens, Hq, Hkv, kv_dtype, num_desc, split_desc):
     """
     bpe = 1 if kv_dtype == "e4m3" else 2
     B = len(seqlens)
-    G = Hq // Hkv
+    rows = q_len * (Hq // Hkv)  # query rows per KV head (q_len query tokens per request)
     kv = sum(seqlens) * Hkv * 128 * 2 * bpe
-    q = B * Hq * 128 * bpe + (B * Hq * 4 if kv_dtype == "e4m3" else 0)
-    part = G * (128 + 1) * 4
-    out = B * Hq * 128 * 2
+    q = B * q_len * Hq * 128 * bpe + (B * q_len * Hq * 4 if kv_dtype == "e4m3" else 0)
+    part = rows * (128 + 1) * 4
+    out = B * q_len * Hq * 128 * 2
     fused = kv + q + out + 2 * split_desc * part
     return {"kv": kv, "q": q, "partials": num_desc * part, "out": out,
             "attn": kv + q + num_desc * part, "combine": num_desc * part + out,
@@ -234,6 +235,7 @@ def parse_args():
     ap.add_argument("--no-static", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue", action="store_true")
+    ap.add_argument("--no-mtp", action="store_true")
     ap.add_argument("--floor", type=int, default=None)
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
@@ -575,6 +577,34 @@ def main():
                          "frac": pre_gbs / peak, "peak_kind": peak_kind}}
         del inp, q_o, qs_o
 
+    # ---- multi-query decode (one draft token, q_len = 2) on the same lengths:
+    # one step reads the KV once for both query tokens
+    mtp = None
+    if not args.no_mtp and 2 * (Hq // Hkv) <= hd.binding.MAX_QUERY_ROWS:
+        import dataclasses
+        w2 = dataclasses.replace(w, q_len=2)
+        b2 = make_batch(w2, device=dev)
+        ws2 = hd.Workspace(B, Hq, Hkv, num_ctas=ctas, device=dev, q_len=2)
+
+        def mtp_step():
+            hd.hpc_decode_step_mq(b2.q, b2.q_scale, b2.k_cache, b2.v_cache, b2.k_scale,
+                                  b2.v_scale, b2.block_table, b2.seqlens, Hq, Hkv, 2, w.sm_scale,
+                                  ctas, floor, 0, ws2.tmap, ws2.part_o, ws2.part_lse, ws2.out,
+                                  unit_done=ws2.unit_done)
+
+        n_m = min(args.steps, 1000)
+        mtp_us = statistics.fmean(timed(n_m, args.warmup, mtp_step))
+        m2 = hd.hpc_decode_read_meta(ws2.tmap)
+        counts2 = ws2.tmap.chunk_count[:B * Hkv].tolist()
+        nb2 = algorithmic_bytes(lens, Hq, Hkv, kv_dtype, m2[2], sum(c for c in counts2 if c > 1),
+                                q_len=2)
+        mtp = {"q_len": 2, "us_per_step": mtp_us, "bytes": nb2["step"],
+               "gbps": nb2["step"] / (mtp_us * 1e-6) / 1e9,
+               "frac": nb2["step"] / (mtp_us * 1e-6) / 1e9 / peak,
+               "two_decode_steps_us": 2 * mean_step,
+               "speedup_vs_two_decode_steps": 2 * mean_step / mtp_us}
+        del b2, ws2
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
@@ -607,6 +637,7 @@ def main():
         "cpu_baseline": cpu_baseline,
         "static": static,
         "rope_norm": prologue,
+        "mtp": mtp,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }

@@ -79,6 +79,7 @@ typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
 #define HPC_PAGE_SIZE 64
 #define HPC_MAX_GROUP 8
 #define HPC_MAX_BATCH 16384
+#define HPC_MAX_QUERY_ROWS 16 /* multi-query decode: q_len * G query rows per KV head at most */
 
 /*
  * Task map: the device-side result of the assign step ([vLLM] Assign bullet;
@@ -253,6 +254,57 @@ hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, cons
 hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
                               const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
                               int32_t head_dim, void *d_out, hpc_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Multi-query decode (q_len > 1: the speculative / MTP layer of Hy3, vLLM
+ * post "A Quick Word on Hy3-series models"; the pages' next-step item of
+ * extend shapes with few query tokens).  Each request's last q_len live
+ * tokens are queries; the caller has written their K and V into the cache
+ * (L_r counts them).  Query token i of request r attends the live tokens
+ * j < L_r - q_len + 1 + i (everything before it and itself).  The task map is
+ * the same as for q_len = 1 (tiles count KV tokens); every descriptor serves
+ * R = q_len * G query rows rho = i * G + g of its KV head, and each KV tile is
+ * read once for all of them.  Layouts:
+ *   q         [B, q_len, Hq, 128]   bf16, or e4m3 with q_scale [B, q_len, Hq]
+ *   out       [B, q_len, Hq, 128]   bf16
+ *   part_o    [cap, R, 128] fp32,   part_lse [cap, R] fp32 (R = q_len * G)
+ * Requires 1 <= q_len and q_len * G <= HPC_MAX_QUERY_ROWS
+ * (HPC_ERR_UNSUPPORTED otherwise).  A query row that sees no token (L_r <
+ * q_len) is written as zeros.  Otherwise as the q_len = 1 calls, which are
+ * these with q_len = 1.
+ * ---------------------------------------------------------------------- */
+hpc_status hpc_decode_attn_mq(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                              const void *d_v_cache, int32_t num_pages, float k_scale,
+                              float v_scale, hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                              int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                              float sm_scale, const hpc_task_map *map, float *d_part_o,
+                              float *d_part_lse, hpc_stream_t stream);
+
+hpc_status hpc_decode_attn_combine_mq(const void *d_q, const float *d_q_scale,
+                                      const void *d_k_cache, const void *d_v_cache,
+                                      int32_t num_pages, float k_scale, float v_scale,
+                                      hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                                      int32_t max_pages_per_req, const int32_t *d_seqlens,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                      int32_t q_len, float sm_scale, const hpc_task_map *map,
+                                      float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
+                                      void *d_out, hpc_stream_t stream);
+
+hpc_status hpc_decode_combine_mq(const float *d_part_o, const float *d_part_lse,
+                                 const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
+                                 int32_t head_dim, int32_t q_len, void *d_out,
+                                 hpc_stream_t stream);
+
+hpc_status hpc_decode_step_mq(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                              const void *d_v_cache, int32_t num_pages, float k_scale,
+                              float v_scale, hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                              int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                              float sm_scale, int32_t num_ctas, int32_t min_tiles_per_cta,
+                              int32_t num_splits, hpc_task_map *map, float *d_part_o,
+                              float *d_part_lse, int32_t *d_unit_done, void *d_out,
+                              hpc_stream_t stream);
 
 /*
  * One whole decode step of one layer on device buffers: hpc_decode_plan

@@ -10,17 +10,20 @@ holds the build step, the ctypes binding and the seeded workload generators.
 
 from .binding import (EXPORTS, HPC_KV_BF16, HPC_KV_FP8_E4M3, HPC_ROPE_HALVES,
                       HPC_ROPE_INTERLEAVED, HpcError, TaskMap, Workspace, hpc_decode_attn,
-                      hpc_decode_attn_combine, hpc_decode_combine, hpc_decode_desc_capacity,
+                      hpc_decode_attn_combine, hpc_decode_attn_combine_mq, hpc_decode_attn_mq,
+                      hpc_decode_combine, hpc_decode_combine_mq, hpc_decode_desc_capacity,
                       hpc_decode_num_ctas, hpc_decode_plan, hpc_decode_plan_static,
                       hpc_decode_read_meta, hpc_decode_static_capacity, hpc_decode_step,
+                      hpc_decode_step_mq,
                       hpc_decode_step_host, hpc_decode_version, hpc_rope_frequencies, hpc_rope_norm,
                       kv_dtype_of, lib)
 
 __all__ = [
     "EXPORTS", "HPC_KV_BF16", "HPC_KV_FP8_E4M3", "HPC_ROPE_HALVES", "HPC_ROPE_INTERLEAVED",
     "HpcError", "TaskMap", "Workspace", "hpc_decode_attn", "hpc_decode_attn_combine",
-    "hpc_decode_combine", "hpc_decode_desc_capacity", "hpc_decode_num_ctas",
+    "hpc_decode_attn_combine_mq", "hpc_decode_attn_mq", "hpc_decode_combine",
+    "hpc_decode_combine_mq", "hpc_decode_desc_capacity", "hpc_decode_num_ctas",
     "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_read_meta",
-    "hpc_decode_static_capacity", "hpc_decode_step", "hpc_decode_step_host",
+    "hpc_decode_static_capacity", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_step_mq",
     "hpc_decode_version", "hpc_rope_frequencies", "hpc_rope_norm", "kv_dtype_of", "lib",
 ]

@@ -18,7 +18,7 @@ from . import _build
 HPC_OK, HPC_ERR_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_WORKSPACE, HPC_ERR_CUDA = 0, -1, -2, -3, -4
 HPC_KV_BF16, HPC_KV_FP8_E4M3 = 0, 1
 HPC_FLAG_BAD_SEQLEN, HPC_FLAG_DESC_OVERFLOW, HPC_FLAG_BAD_PAGE, HPC_FLAG_TIMEOUT = 1, 2, 4, 8
-HEAD_DIM, PAGE_SIZE, MAX_GROUP = 128, 64, 8
+HEAD_DIM, PAGE_SIZE, MAX_GROUP, MAX_QUERY_ROWS = 128, 64, 8, 16
 HPC_ROPE_HALVES, HPC_ROPE_INTERLEAVED = 0, 1
 
 # Every symbol the header declares; the CPU tests check the library exports them all.
@@ -26,7 +26,8 @@ EXPORTS = (
     "hpc_decode_version", "hpc_status_string", "hpc_decode_num_ctas", "hpc_decode_desc_capacity",
     "hpc_decode_static_capacity", "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
-    "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies",
+    "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
+    "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
 )
 
 
@@ -100,6 +101,16 @@ def lib():
                                                    vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
                                                    vp, vp, vp]),
         "hpc_rope_frequencies": (ctypes.c_int, [f32, vp, vp]),
+        "hpc_decode_attn_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp,
+                                              i32, vp, i32, i32, i32, i32, i32, f32, tm, vp, vp,
+                                              vp]),
+        "hpc_decode_attn_combine_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int,
+                                                      vp, i32, vp, i32, i32, i32, i32, i32, f32,
+                                                      tm, vp, vp, vp, vp, vp]),
+        "hpc_decode_combine_mq": (ctypes.c_int, [vp, vp, tm, i32, i32, i32, i32, i32, vp, vp]),
+        "hpc_decode_step_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp,
+                                              i32, vp, i32, i32, i32, i32, i32, f32, i32, i32,
+                                              i32, tm, vp, vp, vp, vp, vp]),
         "hpc_rope_norm": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, vp, i32,
                                          i32, vp, vp, i32, ctypes.c_int, f32, f32, vp, vp, vp,
                                          ctypes.POINTER(hpc_rope_norm_params), vp]),
@@ -261,6 +272,47 @@ def hpc_decode_step(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
         _stream(stream)))
 
 
+def hpc_decode_attn_mq(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens, Hq,
+                       Hkv, q_len, sm_scale, tmap: TaskMap, part_o, part_lse, stream=None):
+    """Multi-query attention: q [B, q_len, Hq, 128]; partials [cap, q_len * G, ...]."""
+    _check("hpc_decode_attn_mq", lib().hpc_decode_attn_mq(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, int(q_len), float(sm_scale), ctypes.byref(tmap.c), _ptr(part_o),
+        _ptr(part_lse), _stream(stream)))
+
+
+def hpc_decode_attn_combine_mq(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                               seqlens, Hq, Hkv, q_len, sm_scale, tmap: TaskMap, part_o, part_lse,
+                               unit_done, out, stream=None):
+    _check("hpc_decode_attn_combine_mq", lib().hpc_decode_attn_combine_mq(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, int(q_len), float(sm_scale), ctypes.byref(tmap.c), _ptr(part_o),
+        _ptr(part_lse), _ptr(unit_done), _ptr(out), _stream(stream)))
+
+
+def hpc_decode_combine_mq(part_o, part_lse, tmap: TaskMap, B, Hq, Hkv, q_len, out, stream=None):
+    _check("hpc_decode_combine_mq", lib().hpc_decode_combine_mq(
+        _ptr(part_o), _ptr(part_lse), ctypes.byref(tmap.c), int(B), int(Hq), int(Hkv), HEAD_DIM,
+        int(q_len), _ptr(out), _stream(stream)))
+
+
+def hpc_decode_step_mq(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, seqlens, Hq,
+                       Hkv, q_len, sm_scale, num_ctas, min_tiles_per_cta, num_splits,
+                       tmap: TaskMap, part_o, part_lse, out, unit_done=None, stream=None):
+    """hpc_decode_step with q_len query tokens per request (causal among them)."""
+    _check("hpc_decode_step_mq", lib().hpc_decode_step_mq(
+        _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]),
+        float(k_scale), float(v_scale), kv_dtype_of(k_cache), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, int(q_len), float(sm_scale), int(num_ctas), int(min_tiles_per_cta),
+        int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(unit_done),
+        _ptr(out), _stream(stream)))
+
+
 def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d_q_scale,
                          d_seqlens, d_block_table, d_out, k_cache, v_cache, k_scale, v_scale, Hq,
                          Hkv, sm_scale, num_ctas, min_tiles_per_cta, num_splits, tmap: TaskMap,
@@ -322,7 +374,7 @@ class Workspace:
     """Split buffer, output and task map sized for one batch shape."""
 
     def __init__(self, B: int, Hq: int, Hkv: int, *, num_ctas: int = 0, num_splits: int = 0,
-                 device="cuda", kv_dtype: int = HPC_KV_BF16):
+                 device="cuda", kv_dtype: int = HPC_KV_BF16, q_len: int = 1):
         dev = torch.device(device)
         if num_splits:
             self.tmap = TaskMap.static(B, Hkv, num_splits, dev)
@@ -331,10 +383,12 @@ class Workspace:
                 num_ctas = hpc_decode_num_ctas(dev.index or 0, kv_dtype)
             self.tmap = TaskMap.dynamic(B, Hkv, num_ctas, dev)
         self.num_ctas, self.num_splits = num_ctas, num_splits
-        G = Hq // Hkv
+        rows = q_len * (Hq // Hkv)  # query rows of one KV head in a descriptor
         cap = max(self.tmap.cap_desc, 1)
-        self.part_o = torch.empty((cap, G, HEAD_DIM), dtype=torch.float32, device=dev)
-        self.part_lse = torch.empty((cap, G), dtype=torch.float32, device=dev)
-        self.out = torch.empty((max(B, 1), Hq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.q_len = q_len
+        self.part_o = torch.empty((cap, rows, HEAD_DIM), dtype=torch.float32, device=dev)
+        self.part_lse = torch.empty((cap, rows), dtype=torch.float32, device=dev)
+        out_shape = (max(B, 1), Hq, HEAD_DIM) if q_len == 1 else (max(B, 1), q_len, Hq, HEAD_DIM)
+        self.out = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
         # chunk counters of the fused combine: zero once, left zero by every launch
         self.unit_done = torch.zeros(max(B * Hkv, 1), dtype=torch.int32, device=dev)

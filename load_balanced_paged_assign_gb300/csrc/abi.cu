@@ -103,8 +103,9 @@ hpc_status make_cache_map(CUtensorMap *m, const void *base, int32_t num_pages, i
     return r == CUDA_SUCCESS ? HPC_OK : HPC_ERR_CUDA;
 }
 
-// Resident CTAs of the attention kernel per device and KV dtype (cached).
-std::atomic<int> g_capacity[kMaxDevices][2];
+// Resident CTAs of the attention kernel per device and variant (KV dtype x
+// row blocks; cached).
+std::atomic<int> g_capacity[kMaxDevices][4];
 
 int resident_ctas(const AttnConfig &cfg, int which) {
     int dev = 0;
@@ -123,10 +124,14 @@ int resident_ctas(const AttnConfig &cfg, int which) {
     return c;
 }
 
-const AttnConfig &config_for(hpc_kv_dtype dt) {
-    static const AttnConfig bf16 = attn_config_bf16();
-    static const AttnConfig fp8 = attn_config_fp8();
-    return dt == HPC_KV_FP8_E4M3 ? fp8 : bf16;
+// Kernel variant: KV dtype x row blocks (nb = 1: up to 8 query rows per KV
+// head, 2: up to 16).
+int variant_of(hpc_kv_dtype dt, int nb) { return (dt == HPC_KV_FP8_E4M3 ? 1 : 0) + 2 * (nb - 1); }
+
+const AttnConfig &config_for(hpc_kv_dtype dt, int nb = 1) {
+    static const AttnConfig cfg[4] = {attn_config_bf16(1), attn_config_fp8(1),
+                                      attn_config_bf16(2), attn_config_fp8(2)};
+    return cfg[variant_of(dt, nb)];
 }
 
 // Shared body of hpc_decode_attn (unit_done == out == nullptr: partials only)
@@ -137,10 +142,12 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
                             int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
                             int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                             const hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                            int32_t *d_unit_done, void *d_out, bool after_plan,
+                            int32_t *d_unit_done, void *d_out, bool after_plan, int32_t q_len,
                             hpc_stream_t stream) {
     hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
     if (st != HPC_OK) return st;
+    if (q_len < 1) return HPC_ERR_ARG;
+    if (q_len * (Hq / Hkv) > HPC_MAX_QUERY_ROWS) return HPC_ERR_UNSUPPORTED;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
     if (num_pages <= 0 || !d_k_cache || !d_v_cache || !d_part_o || !d_part_lse)
@@ -182,15 +189,18 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
     p.G = Hq / Hkv;
     p.max_pages = max_pages_per_req;
     p.num_pages = num_pages;
+    p.q_len = q_len;
+    p.R = q_len * p.G;
     p.score_scale = sm_scale * kLog2eF * (fp8 ? k_scale : 1.f);
     p.v_scale = fp8 ? v_scale : 1.f;
 
-    const AttnConfig &cfg = config_for(kv_dtype);
-    cudaError_t e = prepare_kernel(cfg, fp8 ? 1 : 0);
+    const int nb = p.R > 8 ? 2 : 1;
+    const AttnConfig &cfg = config_for(kv_dtype, nb);
+    cudaError_t e = prepare_kernel(cfg, variant_of(kv_dtype, nb));
     if (e != cudaSuccess) return HPC_ERR_CUDA;
     int grid = map->num_ctas;  // static map: one CTA per bin
     if (map->persistent) {     // persistent: resident CTAs, extra bins pulled dynamically
-        const int cap = resident_ctas(cfg, fp8 ? 1 : 0);
+        const int cap = resident_ctas(cfg, variant_of(kv_dtype, nb));
         if (cap < 1) return HPC_ERR_CUDA;
         grid = std::min(grid, cap);
     }
@@ -204,7 +214,7 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
     // waits.  The map must be load-balanced and planned for this block table.
     p.fly = after_plan && map->persistent && map->max_pages == max_pages_per_req ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = fp8 ? launch_attn_fp8(tk, tv, p, grid, s) : launch_attn_bf16(tk, tv, p, grid, s);
+    e = fp8 ? launch_attn_fp8(nb, tk, tv, p, grid, s) : launch_attn_bf16(nb, tk, tv, p, grid, s);
     return cuda_status(e);
 }
 
@@ -215,7 +225,7 @@ hpc_status attn_combine(const void *d_q, const float *d_q_scale, const void *d_k
                         int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
                         int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                         const hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                        int32_t *d_unit_done, void *d_out, bool after_plan,
+                        int32_t *d_unit_done, void *d_out, bool after_plan, int32_t q_len,
                         hpc_stream_t stream) {
     if (B > 0 && (!d_unit_done || !d_out)) return HPC_ERR_ARG;
     if (!aligned16(d_out)) return HPC_ERR_ARG;
@@ -224,7 +234,24 @@ hpc_status attn_combine(const void *d_q, const float *d_q_scale, const void *d_k
     return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                             kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                             head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
-                            after_plan, stream);
+                            after_plan, q_len, stream);
+}
+
+// hpc_decode_combine_mq's checks and launch.
+hpc_status combine_impl(const float *d_part_o, const float *d_part_lse, const hpc_task_map *map,
+                        int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                        void *d_out, hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, 1);
+    if (st != HPC_OK) return st;
+    if (q_len < 1) return HPC_ERR_ARG;
+    if (q_len * (Hq / Hkv) > HPC_MAX_QUERY_ROWS) return HPC_ERR_UNSUPPORTED;
+    if (!d_part_o || !d_part_lse || (B > 0 && !d_out)) return HPC_ERR_ARG;
+    if (!aligned16(d_part_o) || !aligned16(d_out)) return HPC_ERR_ARG;
+    st = check_map(map, true);
+    if (st != HPC_OK) return st;
+    if (map->B != B || map->Hkv != Hkv || (int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
+    return cuda_status(launch_combine(d_part_o, d_part_lse, *map, B, Hq, Hkv, q_len, d_out,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -324,6 +351,19 @@ hpc_status hpc_decode_plan_static(const int32_t *d_seqlens, int32_t B, int32_t H
     return st;
 }
 
+hpc_status hpc_decode_attn_mq(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                              const void *d_v_cache, int32_t num_pages, float k_scale,
+                              float v_scale, hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                              int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                              float sm_scale, const hpc_task_map *map, float *d_part_o,
+                              float *d_part_lse, hpc_stream_t stream) {
+    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                            head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr,
+                            false, q_len, stream);
+}
+
 hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *d_k_cache,
                            const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
                            hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
@@ -331,10 +371,24 @@ hpc_status hpc_decode_attn(const void *d_q, const float *d_q_scale, const void *
                            int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
                            const hpc_task_map *map, float *d_part_o, float *d_part_lse,
                            hpc_stream_t stream) {
-    return launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
-                            kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
-                            head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr,
-                            false, stream);
+    return hpc_decode_attn_mq(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                              kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                              head_dim, 1, sm_scale, map, d_part_o, d_part_lse, stream);
+}
+
+hpc_status hpc_decode_attn_combine_mq(const void *d_q, const float *d_q_scale,
+                                      const void *d_k_cache, const void *d_v_cache,
+                                      int32_t num_pages, float k_scale, float v_scale,
+                                      hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                                      int32_t max_pages_per_req, const int32_t *d_seqlens,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                      int32_t q_len, float sm_scale, const hpc_task_map *map,
+                                      float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
+                                      void *d_out, hpc_stream_t stream) {
+    return attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                        kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                        head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out, false,
+                        q_len, stream);
 }
 
 hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, const void *d_k_cache,
@@ -345,37 +399,38 @@ hpc_status hpc_decode_attn_combine(const void *d_q, const float *d_q_scale, cons
                                    int32_t head_dim, float sm_scale, const hpc_task_map *map,
                                    float *d_part_o, float *d_part_lse, int32_t *d_unit_done,
                                    void *d_out, hpc_stream_t stream) {
-    return attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
-                        kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
-                        head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out, false,
-                        stream);
+    return hpc_decode_attn_combine_mq(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale,
+                                      v_scale, kv_dtype, d_block_table, max_pages_per_req,
+                                      d_seqlens, B, Hq, Hkv, head_dim, 1, sm_scale, map, d_part_o,
+                                      d_part_lse, d_unit_done, d_out, stream);
+}
+
+hpc_status hpc_decode_combine_mq(const float *d_part_o, const float *d_part_lse,
+                                 const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
+                                 int32_t head_dim, int32_t q_len, void *d_out,
+                                 hpc_stream_t stream) {
+    return combine_impl(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, q_len, d_out, stream);
 }
 
 hpc_status hpc_decode_combine(const float *d_part_o, const float *d_part_lse,
                               const hpc_task_map *map, int32_t B, int32_t Hq, int32_t Hkv,
                               int32_t head_dim, void *d_out, hpc_stream_t stream) {
-    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, 1);
-    if (st != HPC_OK) return st;
-    if (!d_part_o || !d_part_lse || (B > 0 && !d_out)) return HPC_ERR_ARG;
-    if (!aligned16(d_part_o) || !aligned16(d_out)) return HPC_ERR_ARG;
-    st = check_map(map, true);
-    if (st != HPC_OK) return st;
-    if (map->B != B || map->Hkv != Hkv || (int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
-    return cuda_status(launch_combine(d_part_o, d_part_lse, *map, B, Hq, Hkv, d_out,
-                                      static_cast<cudaStream_t>(stream)));
+    return combine_impl(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, 1, d_out, stream);
 }
 
-hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *d_k_cache,
-                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
-                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
-                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
-                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
-                           int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
-                           hpc_task_map *map, float *d_part_o, float *d_part_lse,
-                           int32_t *d_unit_done, void *d_out, hpc_stream_t stream) {
+hpc_status hpc_decode_step_mq(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                              const void *d_v_cache, int32_t num_pages, float k_scale,
+                              float v_scale, hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                              int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                              float sm_scale, int32_t num_ctas, int32_t min_tiles_per_cta,
+                              int32_t num_splits, hpc_task_map *map, float *d_part_o,
+                              float *d_part_lse, int32_t *d_unit_done, void *d_out,
+                              hpc_stream_t stream) {
     hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
     if (st != HPC_OK) return st;
-    if (num_splits < 0) return HPC_ERR_ARG;
+    if (num_splits < 0 || q_len < 1) return HPC_ERR_ARG;
+    if (q_len * (Hq / Hkv) > HPC_MAX_QUERY_ROWS) return HPC_ERR_UNSUPPORTED;
     st = num_splits == 0 ? hpc_decode_plan(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
                                            min_tiles_per_cta, map, stream)
                          : hpc_decode_plan_static(d_seqlens, B, Hkv, max_pages_per_req,
@@ -386,13 +441,27 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
         return attn_combine(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                             kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                             head_dim, sm_scale, map, d_part_o, d_part_lse, d_unit_done, d_out,
-                            true, stream);
+                            true, q_len, stream);
     st = launch_attention(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
                           kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
                           head_dim, sm_scale, map, d_part_o, d_part_lse, nullptr, nullptr, true,
-                          stream);
+                          q_len, stream);
     if (st != HPC_OK) return st;
-    return hpc_decode_combine(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, d_out, stream);
+    return combine_impl(d_part_o, d_part_lse, map, B, Hq, Hkv, head_dim, q_len, d_out, stream);
+}
+
+hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *d_k_cache,
+                           const void *d_v_cache, int32_t num_pages, float k_scale, float v_scale,
+                           hpc_kv_dtype kv_dtype, const int32_t *d_block_table,
+                           int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale,
+                           int32_t num_ctas, int32_t min_tiles_per_cta, int32_t num_splits,
+                           hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                           int32_t *d_unit_done, void *d_out, hpc_stream_t stream) {
+    return hpc_decode_step_mq(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,
+                              kv_dtype, d_block_table, max_pages_per_req, d_seqlens, B, Hq, Hkv,
+                              head_dim, 1, sm_scale, num_ctas, min_tiles_per_cta, num_splits,
+                              map, d_part_o, d_part_lse, d_unit_done, d_out, stream);
 }
 
 hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const int32_t *h_seqlens,

@@ -13,28 +13,41 @@ namespace hpc {
 #endif
 constexpr int kStagesFp8 = HPC_FP8_STAGES;  // pipeline depth (build-time tunable)
 constexpr int kTpsFp8 = HPC_FP8_TPS;        // tiles per stage: 1 or 2
-using TraitsFp8 = AttnTraits<true, kStagesFp8, kTpsFp8>;
+using TraitsFp8 = AttnTraits<true, kStagesFp8, kTpsFp8, 1>;
+// Multi-query decode with 8 < q_len * G <= 16 query rows per KV head: twice
+// the state per consumer, so fewer consumers per stage (one tile) and the
+// ring sized to the remaining shared memory.
+#ifndef HPC_FP8_STAGES_MQ
+#define HPC_FP8_STAGES_MQ 6
+#endif
+constexpr int kStagesFp8Mq = HPC_FP8_STAGES_MQ;
+using TraitsFp8Mq = AttnTraits<true, kStagesFp8Mq, 1, 2>;
 
-AttnConfig attn_config_fp8() {
-    return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8, kTpsFp8>),
+AttnConfig attn_config_fp8(int nb) {
+    if (nb == 2)
+        return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8Mq, 1, 2>),
+                TraitsFp8Mq::kSmemBytes, TraitsFp8Mq::kThreads};
+    return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8, kTpsFp8, 1>),
             TraitsFp8::kSmemBytes, TraitsFp8::kThreads};
 }
 
 // Launched as a programmatic dependent of the previous kernel in the stream
 // (the assign kernel): its prologue overlaps that kernel's tail.
-cudaError_t launch_attn_fp8(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                             int grid, cudaStream_t s) {
+cudaError_t launch_attn_fp8(int nb, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const AttnParams &p, int grid, cudaStream_t s) {
+    const AttnConfig c = attn_config_fp8(nb);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(TraitsFp8::kThreads);
-    cfg.dynamicSmemBytes = TraitsFp8::kSmemBytes;
+    cfg.blockDim = dim3(c.threads);
+    cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8, kTpsFp8>, tk, tv, p);
+    if (nb == 2) return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8Mq, 1, 2>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8, kTpsFp8, 1>, tk, tv, p);
 }
 
 }  // namespace hpc

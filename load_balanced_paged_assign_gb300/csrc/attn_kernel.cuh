@@ -39,6 +39,12 @@
 //  * tiles land with the 128-byte swizzle; every ldmatrix / 16-byte read
 //    touches 8 distinct 16-byte bank groups, and the state hand-off is
 //    lane-major, so it is conflict-free too.
+//  * multi-query decode (q_len > 1, the speculative / MTP layer): a
+//    descriptor serves R = q_len * G query rows (rho = i * G + g) of its KV
+//    head; NB = ceil(R / 8) blocks of 8 rows are the N side of the MMAs, so
+//    every K/V fragment feeds NB MMAs and each KV tile is read once for all
+//    rows.  Query token i sees tokens below L - q_len + 1 + i (per-column
+//    limits in the softmax); NB = 1, q_len = 1 is plain decode.
 //  * the kernel is launched as a programmatic dependent of the assign kernel:
 //    it sets up its barriers, prefetches the block table into L2, derives its
 //    first descriptor from the sequence lengths and starts streaming while
@@ -57,10 +63,10 @@ struct StageInfo {
     int kv_head, req, tile0, ntiles;  // tiles tile0 .. tile0 + ntiles - 1 of request req
     int flags, seqlen, desc_idx, count;  // count: chunks of the unit
     int chunk_off, pad0, pad1, pad2;
-    float qscale[kMaxGroup];
     int pad3[4];
+    float qscale[kMaxRows];  // FP8: scale of query row rho
 };
-static_assert(sizeof(StageInfo) == 96, "StageInfo layout");
+static_assert(sizeof(StageInfo) == 128, "StageInfo layout");
 
 // The fields of a descriptor the combine step needs.
 struct DescInfo {
@@ -78,7 +84,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kCombSlots = 2;   // hand-off slots (double buffer)
-constexpr int kStateRegs = 36;  // per lane: 32 accumulators, m0, m1, l0, l1
+constexpr int kStateRegs = 36;  // per lane and row block: 32 accumulators, m0, m1, l0, l1
 constexpr int kMaxLast = 16;    // split units whose merge this CTA owes, held at once
 constexpr int kStageStride = kHeadDim + 4;  // floats per head row of the combiner's staging
 constexpr int kFlyMaxBatch = 1024;  // largest batch whose first descriptor is derived in-kernel
@@ -94,7 +100,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <bool FP8, int STAGES, int TPS>
+template <bool FP8, int STAGES, int TPS, int NB>
 struct AttnTraits {
     static constexpr int kConsumers = kConsumerWarps * TPS;          // consumer warps
     static constexpr int kThreads = 32 * (2 + kConsumers);           // + producer, combiner
@@ -102,15 +108,17 @@ struct AttnTraits {
     static constexpr int kTileBytes = kTile * kHeadDim * kElem;     // one K or V page, one head
     static constexpr int kHalfBytes = kTile * 64 * 2;               // BF16: one 64-dim half
     static constexpr int kStageKV = TPS * kTileBytes;               // K (or V) bytes per stage
-    static constexpr int kQBytes = kMaxGroup * kHeadDim * kElem;    // Q slot per stage
-    static constexpr int kSlotFloats = kConsumers * kStateRegs * 32;  // one hand-off slot
+    static constexpr int kRows = 8 * NB;                             // query rows held per stage
+    static constexpr int kQBytes = kRows * kHeadDim * kElem;        // Q slot per stage
+    static constexpr int kState = kStateRegs * NB;                   // state floats per lane
+    static constexpr int kSlotFloats = kConsumers * kState * 32;     // one hand-off slot
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + STAGES * kStageKV;
     static constexpr int kOffQ = kOffV + STAGES * kStageKV;
     static constexpr int kOffInfo = kOffQ + STAGES * kQBytes;
     static constexpr int kOffComb = kOffInfo + STAGES * (int)sizeof(StageInfo);
     static constexpr int kOffStage = kOffComb + kCombSlots * kSlotFloats * 4;
-    static constexpr int kOffSlotInfo = kOffStage + kMaxGroup * kStageStride * 4;
+    static constexpr int kOffSlotInfo = kOffStage + kRows * kStageStride * 4;
     static constexpr int kOffLast = kOffSlotInfo + kCombSlots * (int)sizeof(SlotInfo);
     static constexpr int kOffBar = kOffLast + (kMaxLast + 1) * (int)sizeof(SlotInfo);
     // full[STAGES], empty[STAGES], slot full[2], slot empty[2], end rendezvous
@@ -189,29 +197,36 @@ __device__ __forceinline__ bool first_descriptor(const AttnParams &p, int c, int
 // Streams one descriptor (h, r, tb, te) through the stage ring.  desc_idx is
 // its index in the task map, or -1 when it is the first descriptor of bin
 // `bin` derived before the map could be read.  Returns false after a timeout.
-template <bool FP8, int STAGES, int TPS>
+template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                                             const AttnParams &p, uint8_t *smem, int h, int r,
                                             int tb, int te, int desc_idx, int bin,
                                             ProducerState &ps, uint64_t policy,
                                             volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     const int lane = threadIdx.x & 31;
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Tr::kOffInfo);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
     uint64_t *empty = full + STAGES;
-    const uint32_t q_bytes = (uint32_t)(p.G * kHeadDim * Tr::kElem);
+    // Q: the G heads of KV head h for each of the q_len query tokens, stacked
+    // as rows rho = i * G + g (one bulk copy per query token)
+    const uint32_t q_group = (uint32_t)(p.G * kHeadDim * Tr::kElem);
+    const uint32_t q_bytes = q_group * (uint32_t)p.q_len;
+    const size_t q_token_stride = (size_t)p.Hq * kHeadDim * Tr::kElem;
     if (tb >= te) return true;  // empty split of the static schedule
     const int L = p.seqlens[r];
     const int u = h * p.B + r;
     float qs = 1.f;
-    if (FP8 && lane < p.G) qs = p.q_scale[(size_t)r * p.Hq + h * p.G + lane];
-    float qsg[kMaxGroup];
+    if (FP8 && lane < p.R) {
+        const int i = lane / p.G;
+        qs = p.q_scale[((size_t)r * p.q_len + i) * p.Hq + h * p.G + (lane - i * p.G)];
+    }
+    float qsg[Tr::kRows];
 #pragma unroll
-    for (int g = 0; g < kMaxGroup; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
+    for (int g = 0; g < Tr::kRows; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
     const int32_t *bt_row = p.block_table + (size_t)r * p.max_pages;
     const uint8_t *q_src = static_cast<const uint8_t *>(p.q) +
-                           ((size_t)r * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
+                           ((size_t)r * p.q_len * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
 
     for (int t0 = tb; t0 < te; t0 += 32) {  // 32 block-table entries at a time
         const int nt = min(32, te - t0);
@@ -255,7 +270,7 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                 si.count = count;
                 si.chunk_off = chunk_off;
 #pragma unroll
-                for (int g = 0; g < kMaxGroup; ++g) si.qscale[g] = qsg[g];
+                for (int g = 0; g < Tr::kRows; ++g) si.qscale[g] = qsg[g];
                 mbar_arrive_expect_tx(&full[stage], 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u));
 #pragma unroll
                 for (int s = 0; s < TPS; ++s) {
@@ -276,7 +291,9 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                     }
                 }
                 if (first)
-                    bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes, q_src, q_bytes, &full[stage]);
+                    for (int i = 0; i < p.q_len; ++i)
+                        bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes + i * q_group,
+                                  q_src + i * q_token_stride, q_group, &full[stage]);
             }
             __syncwarp();
             ++ps.it;
@@ -285,11 +302,11 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
     return true;
 }
 
-template <bool FP8, int STAGES, int TPS>
+template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                                               const AttnParams &p, uint8_t *smem,
                                               volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     const int lane = threadIdx.x & 31;
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Tr::kOffInfo);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
@@ -307,7 +324,7 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     if (p.fly) {
         int h, r, tb, te;
         if (first_descriptor(p, blockIdx.x, h, r, tb, te) && te > tb) {
-            ok = stream_desc<FP8, STAGES, TPS>(tmap_k, tmap_v, p, smem, h, r, tb, te, -1,
+            ok = stream_desc<FP8, STAGES, TPS, NB>(tmap_k, tmap_v, p, smem, h, r, tb, te, -1,
                                                blockIdx.x, ps, policy, abort);
             skip = 1;
         }
@@ -326,7 +343,7 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
         const int d_end = p.bin_ptr[bin + 1];
         for (int d = d_begin; d < d_end && ok; ++d) {
             const int4 ds = p.desc[d];
-            ok = stream_desc<FP8, STAGES, TPS>(tmap_k, tmap_v, p, smem, ds.x, ds.y, ds.z, ds.w, d,
+            ok = stream_desc<FP8, STAGES, TPS, NB>(tmap_k, tmap_v, p, smem, ds.x, ds.y, ds.z, ds.w, d,
                                                bin, ps, policy, abort);
         }
         if (!dynamic) break;
@@ -361,22 +378,24 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     __syncwarp();
 }
 
-// Merge of split unit `di` for query head hd by one warp: lane l owns dims
-// 4l .. 4l + 3; LSEs are read lane-parallel and their weights broadcast by
-// shuffle, with eight partial rows in flight at a time.
-__device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescInfo &di, int hd) {
+// Merge of split unit `di` for query row rho (= i * G + g) by one warp: lane l
+// owns dims 4l .. 4l + 3; LSEs are read lane-parallel and their weights
+// broadcast by shuffle, with eight partial rows in flight at a time.  A row
+// that sees no token in any chunk (multi-query rows of a request shorter
+// than q_len) is written as zeros.
+__device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescInfo &di, int rho) {
     const int lane = threadIdx.x & 31;
-    const float *lse = p.part_lse + (size_t)di.chunk_off * p.G + hd;
+    const float *lse = p.part_lse + (size_t)di.chunk_off * p.R + rho;
     const float4 *po = reinterpret_cast<const float4 *>(
-                           p.part_o + ((size_t)di.chunk_off * p.G + hd) * kHeadDim) + lane;
-    const size_t row = (size_t)p.G * kHeadDim / 4;  // float4s between chunk rows
+                           p.part_o + ((size_t)di.chunk_off * p.R + rho) * kHeadDim) + lane;
+    const size_t row = (size_t)p.R * kHeadDim / 4;  // float4s between chunk rows
     float4 x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         x[j] = j < di.count ? __ldcg(po + (size_t)j * row) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float lv0 = lane < di.count ? __ldcg(lse + (size_t)lane * p.G) : kNegInf;
+    const float lv0 = lane < di.count ? __ldcg(lse + (size_t)lane * p.R) : kNegInf;
     float m = lv0;
-    for (int i = 32 + lane; i < di.count; i += 32) m = fmaxf(m, __ldcg(lse + (size_t)i * p.G));
+    for (int i = 32 + lane; i < di.count; i += 32) m = fmaxf(m, __ldcg(lse + (size_t)i * p.R));
 #pragma unroll
     for (int o_ = 16; o_ > 0; o_ >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o_));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -385,7 +404,7 @@ __device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescI
         const int cnt = min(32, di.count - base);
         float wl = 0.f;
         if (lane < cnt)
-            wl = ex2(((base ? __ldcg(lse + (size_t)(base + lane) * p.G) : lv0) - m) * kLog2e);
+            wl = ex2(((base ? __ldcg(lse + (size_t)(base + lane) * p.R) : lv0) - m) * kLog2e);
         float ws = wl;
 #pragma unroll
         for (int o_ = 16; o_ > 0; o_ >>= 1) ws += __shfl_xor_sync(kFullMask, ws, o_);
@@ -405,9 +424,12 @@ __device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescI
             }
         }
     }
-    const float inv = 1.f / wsum;
+    const float inv = m == kNegInf ? 0.f : 1.f / wsum;
+    if (inv == 0.f) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int qi = rho / p.G;
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) +
-                         ((size_t)di.req * p.Hq + di.kv_head * p.G + hd) * kHeadDim + 4 * lane;
+                         (((size_t)di.req * p.q_len + qi) * p.Hq + di.kv_head * p.G +
+                          (rho - qi * p.G)) * kHeadDim + 4 * lane;
     *reinterpret_cast<uint2 *>(dst) =
         make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
@@ -431,10 +453,10 @@ __device__ __forceinline__ int stage_col(int dim) { return dim ^ (((dim >> 4) & 
 
 // Merges the consumers' states of each finished descriptor and writes the
 // result; counts chunks of split units.  Returns false after a timeout.
-template <bool FP8, int STAGES, int TPS>
+template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem,
                                               volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     constexpr int NC = Tr::kConsumers;
     const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
     const float *comb = reinterpret_cast<const float *>(smem + Tr::kOffComb);
@@ -451,72 +473,89 @@ __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem
         if (!warp_wait(&slot_full[k], (n / kCombSlots) & 1u, abort)) return false;
         const SlotInfo si = slots[k];
         if (si.flags & kEnd) break;
-        // [warp][lane][36]: this lane's 9 float4 of every consumer warp
-        const float4 *st = reinterpret_cast<const float4 *>(comb + k * Tr::kSlotFloats) + lane * 9;
-        float4 ml[NC];
-        float M0 = kNegInf, M1 = kNegInf;
+        // [warp][lane][36 NB]: this lane's 9 NB float4 of every consumer warp;
+        // row block nb holds rows 8 nb + (2 t4, 2 t4 + 1) of this lane
+        const float4 *st = reinterpret_cast<const float4 *>(comb + k * Tr::kSlotFloats) +
+                           lane * 9 * NB;
+        float lse_l[NB][2];  // natural-log LSE of this lane's two rows of each block
 #pragma unroll
-        for (int w = 0; w < NC; ++w) {
-            ml[w] = st[w * 32 * 9 + 8];  // (m0, m1, l0, l1)
-            M0 = fmaxf(M0, ml[w].x);
-            M1 = fmaxf(M1, ml[w].y);
-        }
-        const float Z0 = M0 == kNegInf ? 0.f : M0, Z1 = M1 == kNegInf ? 0.f : M1;
-        float acc[32], L0 = 0.f, L1 = 0.f;
+        for (int nb = 0; nb < NB; ++nb) {
+            float4 ml[NC];
+            float M0 = kNegInf, M1 = kNegInf;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) acc[r] = 0.f;
-#pragma unroll
-        for (int w = 0; w < NC; ++w) {
-            const float a0 = ex2(ml[w].x - Z0), a1 = ex2(ml[w].y - Z1);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = st[w * 32 * 9 + j];
-                acc[4 * j + 0] += v.x * a0;
-                acc[4 * j + 1] += v.y * a1;
-                acc[4 * j + 2] += v.z * a0;
-                acc[4 * j + 3] += v.w * a1;
+            for (int w = 0; w < NC; ++w) {
+                ml[w] = st[w * 32 * 9 * NB + nb * 9 + 8];  // (m0, m1, l0, l1)
+                M0 = fmaxf(M0, ml[w].x);
+                M1 = fmaxf(M1, ml[w].y);
             }
-            L0 += ml[w].z * a0;
-            L1 += ml[w].w * a1;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&slot_empty[k]);  // the consumers may refill the slot
+            const float Z0 = M0 == kNegInf ? 0.f : M0, Z1 = M1 == kNegInf ? 0.f : M1;
+            float acc[32], L0 = 0.f, L1 = 0.f;
 #pragma unroll
-        for (int o_ = 4; o_ <= 16; o_ <<= 1) {  // per-head sums over the tokens of all lanes
-            L0 += __shfl_xor_sync(kFullMask, L0, o_);
-            L1 += __shfl_xor_sync(kFullMask, L1, o_);
-        }
-        const float inv0 = p.v_scale / L0, inv1 = p.v_scale / L1;
-        // stage the normalised result as [head][dim] for coalesced stores
+            for (int r = 0; r < 32; ++r) acc[r] = 0.f;
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-            stage[(2 * t4 + (r & 1)) * kStageStride + stage_col(state_dim<FP8>(r, g))] =
-                acc[r] * ((r & 1) ? inv1 : inv0);
+            for (int w = 0; w < NC; ++w) {
+                const float a0 = ex2(ml[w].x - Z0), a1 = ex2(ml[w].y - Z1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 v = st[w * 32 * 9 * NB + nb * 9 + j];
+                    acc[4 * j + 0] += v.x * a0;
+                    acc[4 * j + 1] += v.y * a1;
+                    acc[4 * j + 2] += v.z * a0;
+                    acc[4 * j + 3] += v.w * a1;
+                }
+                L0 += ml[w].z * a0;
+                L1 += ml[w].w * a1;
+            }
+            if (nb == NB - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_empty[k]);  // the consumers may refill the slot
+            }
+#pragma unroll
+            for (int o_ = 4; o_ <= 16; o_ <<= 1) {  // per-row sums over the tokens of all lanes
+                L0 += __shfl_xor_sync(kFullMask, L0, o_);
+                L1 += __shfl_xor_sync(kFullMask, L1, o_);
+            }
+            // a row that saw no token (L = 0) is a zero row with LSE -inf
+            const float inv0 = L0 > 0.f ? p.v_scale / L0 : 0.f;
+            const float inv1 = L1 > 0.f ? p.v_scale / L1 : 0.f;
+            lse_l[nb][0] = L0 > 0.f ? (Z0 + lg2(L0)) * kLn2 : kNegInf;
+            lse_l[nb][1] = L1 > 0.f ? (Z1 + lg2(L1)) * kLn2 : kNegInf;
+            // stage the normalised result as [row][dim] for coalesced stores
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                stage[(8 * nb + 2 * t4 + (r & 1)) * kStageStride + stage_col(state_dim<FP8>(r, g))] =
+                    acc[r] * ((r & 1) ? inv1 : inv0);
+        }
         __syncwarp();
         const DescInfo di = si.di;
         const bool direct = fused && di.count == 1;
         if (direct) {  // the unit's only chunk: final BF16 output
-            for (int h = 0; h < p.G; ++h) {
-                const float4 v =
-                    *reinterpret_cast<const float4 *>(stage + h * kStageStride + stage_col(4 * lane));
+            for (int rho = 0; rho < p.R; ++rho) {
+                const float4 v = *reinterpret_cast<const float4 *>(stage + rho * kStageStride +
+                                                                   stage_col(4 * lane));
+                const int qi = rho / p.G;
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) +
-                                     ((size_t)di.req * p.Hq + di.kv_head * p.G + h) * kHeadDim;
+                                     (((size_t)di.req * p.q_len + qi) * p.Hq + di.kv_head * p.G +
+                                      (rho - qi * p.G)) * kHeadDim;
                 reinterpret_cast<uint2 *>(dst)[lane] =
                     make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
             }
         } else {  // partial + LSE, kept in L2 for the CTA (or kernel) that merges
             const uint64_t keep = policy_evict_last();
-            for (int h = 0; h < p.G; ++h) {
-                const float4 v =
-                    *reinterpret_cast<const float4 *>(stage + h * kStageStride + stage_col(4 * lane));
-                float *dst = p.part_o + ((size_t)di.desc_idx * p.G + h) * kHeadDim;
+            for (int rho = 0; rho < p.R; ++rho) {
+                const float4 v = *reinterpret_cast<const float4 *>(stage + rho * kStageStride +
+                                                                   stage_col(4 * lane));
+                float *dst = p.part_o + ((size_t)di.desc_idx * p.R + rho) * kHeadDim;
                 st_global_hint(reinterpret_cast<float4 *>(dst) + lane, v, keep);
             }
             if (g == 0) {
-                const float lse0 = (Z0 + lg2(L0)) * kLn2, lse1 = (Z1 + lg2(L1)) * kLn2;
-                float *dl = p.part_lse + (size_t)di.desc_idx * p.G;
-                if (2 * t4 < p.G) st_global_hint(dl + 2 * t4, lse0, keep);
-                if (2 * t4 + 1 < p.G) st_global_hint(dl + 2 * t4 + 1, lse1, keep);
+                float *dl = p.part_lse + (size_t)di.desc_idx * p.R;
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const int rho = 8 * nb + 2 * t4;
+                    if (rho < p.R) st_global_hint(dl + rho, lse_l[nb][0], keep);
+                    if (rho + 1 < p.R) st_global_hint(dl + rho + 1, lse_l[nb][1], keep);
+                }
             }
             if (fused) {  // count this chunk of a split unit
                 __syncwarp();  // every lane's partial stores precede lane 0's release below
@@ -534,7 +573,7 @@ __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem
                         if (lane == 0) last[1 + nlast].di = di;
                         ++nlast;
                     } else {  // list full (many bins per CTA): merge here, alone
-                        for (int h = 0; h < p.G; ++h) merge_unit_head(p, di, h);
+                        for (int rho = 0; rho < p.R; ++rho) merge_unit_head(p, di, rho);
                     }
                 }
             }
@@ -546,10 +585,10 @@ __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem
 }
 
 // ------------------------------------------------------------------ consumer
-template <bool FP8, int STAGES, int TPS>
+template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem,
                                               volatile int *abort) {
-    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     const int lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 2;
     const int g = lane >> 2, t4 = lane & 3;
     const int slot = cw >> 2;  // which tile of the stage this warp works on
@@ -569,13 +608,25 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
     const int tok_k = 16 * sub + (lane & 7) + (mi & 1) * 8;  // K: matrices 1, 3 = rows 8..15
     const int tok_v = 16 * sub + (lane & 7) + (mi >> 1) * 8;  // V^T: matrices 2, 3 = toks 8..15
 
-    float o[8][4];
-    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f, sc0 = 0.f, sc1 = 0.f;
-    uint32_t qf[8][2];
+    // Row block nb holds query rows 8 nb .. 8 nb + 7; this lane owns columns
+    // (rows) 8 nb + 2 t4 + c, c = 0, 1 of every block.
+    float o[NB][8][4];
+    float m[NB][2], l[NB][2], sc[NB][2];
+    int lim[NB][2];  // tokens visible to the lane's rows: t < lim (causal for q_len > 1)
+    uint32_t qf[NB][8][2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        qf[j][0] = qf[j][1] = 0u;
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            m[nb][c] = kNegInf;
+            l[nb][c] = sc[nb][c] = 0.f;
+            lim[nb][c] = 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            o[nb][j][0] = o[nb][j][1] = o[nb][j][2] = o[nb][j][3] = 0.f;
+            qf[nb][j][0] = qf[nb][j][1] = 0u;
+        }
     }
 
     uint32_t handed = 0;  // descriptors handed to the combiner
@@ -592,115 +643,161 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
 
         if (!(flags & kEnd)) {
             if (flags & kFirst) {  // new descriptor: load Q^T fragments, reset the state
-                // B fragment of Q^T (k = dim, n = head): lane holds head g, dims
+                // B fragment of Q^T (k = dim, n = row): lane holds row 8 nb + g, dims
                 // 2t4.. (bf16) or 4t4.. (e4m3) of each k-step, and +8 / +16 beyond.
-                const uint8_t *q = smem + Tr::kOffQ + stage * Tr::kQBytes + g * kHeadDim * Tr::kElem;
-                const bool live = g < p.G;
-    #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    if (FP8 && s >= 4) break;
-                    const int off = FP8 ? 32 * s + 4 * t4 : 2 * (16 * s + 2 * t4);
-                    qf[s][0] = live ? *reinterpret_cast<const uint32_t *>(q + off) : 0u;
-                    qf[s][1] = live ? *reinterpret_cast<const uint32_t *>(q + off + 16) : 0u;
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const int row = 8 * nb + g;
+                    const uint8_t *q =
+                        smem + Tr::kOffQ + stage * Tr::kQBytes + row * kHeadDim * Tr::kElem;
+                    const bool live = row < p.R;
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        if (FP8 && s >= 4) break;
+                        const int off = FP8 ? 32 * s + 4 * t4 : 2 * (16 * s + 2 * t4);
+                        qf[nb][s][0] = live ? *reinterpret_cast<const uint32_t *>(q + off) : 0u;
+                        qf[nb][s][1] = live ? *reinterpret_cast<const uint32_t *>(q + off + 16) : 0u;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int rho = 8 * nb + 2 * t4 + c;
+                        sc[nb][c] = p.score_scale * info[stage].qscale[rho];
+                        // query token i = rho / G sees tokens below L - q_len + 1 + i
+                        lim[nb][c] = rho < p.R ? L - p.q_len + 1 + rho / p.G : L;
+                        m[nb][c] = kNegInf;
+                        l[nb][c] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        o[nb][j][0] = o[nb][j][1] = o[nb][j][2] = o[nb][j][3] = 0.f;
                 }
-                sc0 = p.score_scale * info[stage].qscale[2 * t4];
-                sc1 = p.score_scale * info[stage].qscale[2 * t4 + 1];
-                m0 = m1 = kNegInf;
-                l0 = l1 = 0.f;
-    #pragma unroll
-                for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             }
 
             if (slot < ntiles) {
                 const uint32_t sK = sK0 + stage * Tr::kStageKV, sV = sV0 + stage * Tr::kStageKV;
                 const int tile = tile0 + slot;
 
-                // ---- S^T = K . Q^T for this warp's 16 tokens x 8 heads
-                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                // ---- S^T = K . Q^T for this warp's 16 tokens x 8 NB rows
+                float s4[NB][4];
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) s4[nb][0] = s4[nb][1] = s4[nb][2] = s4[nb][3] = 0.f;
                 if (FP8) {
-    #pragma unroll
+#pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const int chunk = 2 * s + (mi >> 1);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(sK + tok_k * 128 + ((chunk ^ (tok_k & 7)) << 4), a0, a1, a2, a3);
-                        mma_e4m3_16832(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+                            mma_e4m3_16832(s4[nb], a0, a1, a2, a3, qf[nb][s][0], qf[nb][s][1]);
                     }
                 } else {
-                    float s4b[4] = {0.f, 0.f, 0.f, 0.f};  // two chains: even / odd k-steps
-    #pragma unroll
+                    float s4b[NB][4];  // two chains: even / odd k-steps
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+                        s4b[nb][0] = s4b[nb][1] = s4b[nb][2] = s4b[nb][3] = 0.f;
+#pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         const int chunk = (2 * s + (mi >> 1)) & 7;
                         const uint32_t addr = sK + (s >> 2) * Tr::kHalfBytes + tok_k * 128 +
                                               ((chunk ^ (tok_k & 7)) << 4);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(addr, a0, a1, a2, a3);
-                        if (s & 1)
-                            mma_bf16_16816(s4b, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                        else
-                            mma_bf16_16816(s4, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb) {
+                            if (s & 1)
+                                mma_bf16_16816(s4b[nb], a0, a1, a2, a3, qf[nb][s][0], qf[nb][s][1]);
+                            else
+                                mma_bf16_16816(s4[nb], a0, a1, a2, a3, qf[nb][s][0], qf[nb][s][1]);
+                        }
                     }
-    #pragma unroll
-                    for (int e = 0; e < 4; ++e) s4[e] += s4b[e];
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s4[nb][e] += s4b[nb][e];
                 }
 
-                // ---- online softmax (log2 domain); tokens at or past L are masked
+                // ---- online softmax (log2 domain); a token at or past a row's
+                // limit is masked for that row
                 const int tok0 = tile * kTile + 16 * sub;  // first token of this warp's slice
-                const bool va = tok0 + g < L, vb = tok0 + g + 8 < L;
-                const float x0 = va ? s4[0] * sc0 : kNegInf, x1 = va ? s4[1] * sc1 : kNegInf;
-                const float x2 = vb ? s4[2] * sc0 : kNegInf, x3 = vb ? s4[3] * sc1 : kNegInf;
-                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-    #pragma unroll
-                for (int o_ = 4; o_ <= 16; o_ <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, o_));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, o_));
+                const int ta = tok0 + g, tb_ = tok0 + g + 8;
+                float x[NB][4], mx[NB][2];
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    x[nb][0] = ta < lim[nb][0] ? s4[nb][0] * sc[nb][0] : kNegInf;
+                    x[nb][1] = ta < lim[nb][1] ? s4[nb][1] * sc[nb][1] : kNegInf;
+                    x[nb][2] = tb_ < lim[nb][0] ? s4[nb][2] * sc[nb][0] : kNegInf;
+                    x[nb][3] = tb_ < lim[nb][1] ? s4[nb][3] * sc[nb][1] : kNegInf;
+                    mx[nb][0] = fmaxf(x[nb][0], x[nb][2]);
+                    mx[nb][1] = fmaxf(x[nb][1], x[nb][3]);
                 }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float ms0 = mn0 == kNegInf ? 0.f : mn0, ms1 = mn1 == kNegInf ? 0.f : mn1;
-                const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
-                m0 = mn0;
-                m1 = mn1;
-                const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-                const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-                uint32_t pk01, pk23;
-                if (FP8) {
-                    pk01 = pack_f16x2(p0, p1);
-                    pk23 = pack_f16x2(p2, p3);
-                    const float2 r01 = f16x2_to_f32x2(pk01), r23 = f16x2_to_f32x2(pk23);
-                    l0 = l0 * al0 + r01.x + r23.x;
-                    l1 = l1 * al1 + r01.y + r23.y;
-                } else {
-                    pk01 = pack_bf16x2(p0, p1);
-                    pk23 = pack_bf16x2(p2, p3);
-                    l0 = l0 * al0 + bf16lo_to_f32(pk01) + bf16lo_to_f32(pk23);
-                    l1 = l1 * al1 + bf16hi_to_f32(pk01) + bf16hi_to_f32(pk23);
-                }
-                if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {  // rescale only on a new max
-    #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        o[j][0] *= al0;
-                        o[j][1] *= al1;
-                        o[j][2] *= al0;
-                        o[j][3] *= al1;
+#pragma unroll
+                for (int o_ = 4; o_ <= 16; o_ <<= 1)
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        mx[nb][0] = fmaxf(mx[nb][0], __shfl_xor_sync(kFullMask, mx[nb][0], o_));
+                        mx[nb][1] = fmaxf(mx[nb][1], __shfl_xor_sync(kFullMask, mx[nb][1], o_));
                     }
+                float al[NB][2];
+                bool rescale = false;
+                uint32_t b0[NB], b1[NB];
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    float ms[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const float mn = fmaxf(m[nb][c], mx[nb][c]);
+                        ms[c] = mn == kNegInf ? 0.f : mn;
+                        al[nb][c] = ex2(m[nb][c] - ms[c]);
+                        m[nb][c] = mn;
+                        rescale |= al[nb][c] != 1.f;
+                    }
+                    const float p0 = ex2(x[nb][0] - ms[0]), p1 = ex2(x[nb][1] - ms[1]);
+                    const float p2 = ex2(x[nb][2] - ms[0]), p3 = ex2(x[nb][3] - ms[1]);
+                    uint32_t pk01, pk23;
+                    if (FP8) {
+                        pk01 = pack_f16x2(p0, p1);
+                        pk23 = pack_f16x2(p2, p3);
+                        const float2 r01 = f16x2_to_f32x2(pk01), r23 = f16x2_to_f32x2(pk23);
+                        l[nb][0] = l[nb][0] * al[nb][0] + r01.x + r23.x;
+                        l[nb][1] = l[nb][1] * al[nb][1] + r01.y + r23.y;
+                    } else {
+                        pk01 = pack_bf16x2(p0, p1);
+                        pk23 = pack_bf16x2(p2, p3);
+                        l[nb][0] = l[nb][0] * al[nb][0] + bf16lo_to_f32(pk01) + bf16lo_to_f32(pk23);
+                        l[nb][1] = l[nb][1] * al[nb][1] + bf16hi_to_f32(pk01) + bf16hi_to_f32(pk23);
+                    }
+                    // P^T fragments (k = token, n = row): transpose the 8x8 halves
+                    b0[nb] = movmatrix_trans(pk01);
+                    b1[nb] = movmatrix_trans(pk23);
                 }
-                // P^T fragments (k = token, n = head): transpose the 8x8 halves
-                const uint32_t b0 = movmatrix_trans(pk01), b1 = movmatrix_trans(pk23);
+                if (__any_sync(kFullMask, rescale)) {  // rescale only on a new max
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            o[nb][j][0] *= al[nb][0];
+                            o[nb][j][1] *= al[nb][1];
+                            o[nb][j][2] *= al[nb][0];
+                            o[nb][j][3] *= al[nb][1];
+                        }
+                }
 
-                // ---- O^T += V^T . P^T
+                // ---- O^T += V^T . P^T (one V fragment feeds every row block)
                 if (FP8) {
                     // rows 2t4, 2t4+1, 2t4+8, 2t4+9 of the slice; dims 16g .. 16g+15
-                    uint4 R[4];
-    #pragma unroll
+                    uint4 Rv[4];
+#pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int tok = 16 * sub + 2 * t4 + (q & 1) + (q >> 1) * 8;
-                        R[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
-                        if (tile * kTile + tok >= L) R[q] = make_uint4(0u, 0u, 0u, 0u);
+                        Rv[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
+                        if (tile * kTile + tok >= L) Rv[q] = make_uint4(0u, 0u, 0u, 0u);
                     }
-                    const uint32_t wA[4] = {R[0].x, R[0].y, R[0].z, R[0].w};
-                    const uint32_t wB[4] = {R[1].x, R[1].y, R[1].z, R[1].w};
-                    const uint32_t wC[4] = {R[2].x, R[2].y, R[2].z, R[2].w};
-                    const uint32_t wD[4] = {R[3].x, R[3].y, R[3].z, R[3].w};
-    #pragma unroll
+                    const uint32_t wA[4] = {Rv[0].x, Rv[0].y, Rv[0].z, Rv[0].w};
+                    const uint32_t wB[4] = {Rv[1].x, Rv[1].y, Rv[1].z, Rv[1].w};
+                    const uint32_t wC[4] = {Rv[2].x, Rv[2].y, Rv[2].z, Rv[2].w};
+                    const uint32_t wD[4] = {Rv[3].x, Rv[3].y, Rv[3].z, Rv[3].w};
+#pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
                         const uint32_t x01 = __byte_perm(wA[j >> 1], wB[j >> 1], sel);
@@ -708,7 +805,9 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
                         uint32_t a0, a1, a2, a3;
                         e4m3x4_to_f16x2x2(x01, a0, a1);
                         e4m3x4_to_f16x2x2(x23, a2, a3);
-                        mma_f16_16816(o[j], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+                            mma_f16_16816(o[nb][j], a0, a1, a2, a3, b0[nb], b1[nb]);
                     }
                 } else {
                     const int tv = tok0 + 2 * t4;  // tokens of a0/a1 halves; +8 for a2/a3
@@ -716,14 +815,17 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
                         (tv < L ? 0x0000ffffu : 0u) | (tv + 1 < L ? 0xffff0000u : 0u);
                     const uint32_t mk23 =
                         (tv + 8 < L ? 0x0000ffffu : 0u) | (tv + 9 < L ? 0xffff0000u : 0u);
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int chunk = (2 * j + (mi & 1)) & 7;
                         const uint32_t addr = sV + (j >> 2) * Tr::kHalfBytes + tok_v * 128 +
                                               ((chunk ^ (tok_v & 7)) << 4);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_trans(addr, a0, a1, a2, a3);
-                        mma_bf16_16816(o[j], a0 & mk01, a1 & mk01, a2 & mk23, a3 & mk23, b0, b1);
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+                            mma_bf16_16816(o[nb][j], a0 & mk01, a1 & mk01, a2 & mk23, a3 & mk23,
+                                           b0[nb], b1[nb]);
                     }
                 }
             }
@@ -735,12 +837,17 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
             const int k = handed % kCombSlots;
             if (!warp_wait(&slot_empty[k], ((handed / kCombSlots) & 1u) ^ 1u, abort))
                 return false;
-            if (flags & kLast) {  // lane-major: 9 float4 per lane, conflict-free
+            if (flags & kLast) {  // lane-major: 9 NB float4 per lane, conflict-free
                 float4 *dst = reinterpret_cast<float4 *>(
-                    comb + ((k * Tr::kConsumers + cw) * 32 + lane) * kStateRegs);
+                    comb + ((k * Tr::kConsumers + cw) * 32 + lane) * Tr::kState);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
-                dst[8] = make_float4(m0, m1, l0, l1);
+                for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[9 * nb + j] =
+                            make_float4(o[nb][j][0], o[nb][j][1], o[nb][j][2], o[nb][j][3]);
+                    dst[9 * nb + 8] = make_float4(m[nb][0], m[nb][1], l[nb][0], l[nb][1]);
+                }
                 if (cw == 0 && lane == 0) slots[k] = SlotInfo{di, 0, 0, 0};
             } else if (cw == 0 && lane == 0) {
                 slots[k].flags = kEnd;
@@ -753,11 +860,11 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool FP8, int STAGES, int TPS>
-__global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
+template <bool FP8, int STAGES, int TPS, int NB>
+__global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
-    using Tr = AttnTraits<FP8, STAGES, TPS>;
+    using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
@@ -784,7 +891,7 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
     // may still be running.
     {
         const size_t bt_bytes = (size_t)p.B * p.max_pages * 4;
-        const size_t q_bytes = (size_t)p.B * p.Hq * kHeadDim * Tr::kElem;
+        const size_t q_bytes = (size_t)p.B * p.q_len * p.Hq * kHeadDim * Tr::kElem;
         const char *bt = reinterpret_cast<const char *>(p.block_table);
         const char *q = static_cast<const char *>(p.q);
         for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 128; off < bt_bytes;
@@ -800,7 +907,7 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
-        attn_producer<FP8, STAGES, TPS>(&tmap_k, &tmap_v, p, smem, abort);
+        attn_producer<FP8, STAGES, TPS, NB>(&tmap_k, &tmap_v, p, smem, abort);
         return;
     }
     // Every global write of this grid (outputs, partials, counters) comes
@@ -808,16 +915,16 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
     // until the first hand-off, waits here; the end phase waits below.
     if (warp == 1) grid_dependency_wait();
     if (warp == 1 && p.out) {  // fused mode: requests without live tokens get zero rows
-        const int row_vec = p.Hq * kHeadDim * 2 / 16;  // 16-byte vectors per request
+        const int row_vec = p.q_len * p.Hq * kHeadDim * 2 / 16;  // 16-byte vectors per request
         for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
             if (p.seqlens[r] > 0) continue;
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                   (size_t)r * p.Hq * kHeadDim);
+                                                   (size_t)r * p.q_len * p.Hq * kHeadDim);
             for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
         }
     }
-    bool ok = warp == 1 ? attn_combiner<FP8, STAGES, TPS>(p, smem, abort)
-                        : attn_consumer<FP8, STAGES, TPS>(p, smem, abort);
+    bool ok = warp == 1 ? attn_combiner<FP8, STAGES, TPS, NB>(p, smem, abort)
+                        : attn_consumer<FP8, STAGES, TPS, NB>(p, smem, abort);
     if (!ok) {
         grid_dependency_wait();  // meta[3] is written by the assign kernel
         if (lane == 0) atomicOr(p.meta + 3, (int)HPC_FLAG_TIMEOUT);
@@ -838,8 +945,8 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS>::kThreads, 1)
     const SlotInfo *last = reinterpret_cast<const SlotInfo *>(smem + Tr::kOffLast);
     const int nlast = last[0].flags;
     const int nw = 1 + Tr::kConsumers, w = warp - 1;
-    for (int item = w; item < nlast * p.G; item += nw)
-        merge_unit_head(p, last[1 + item / p.G].di, item % p.G);
+    for (int item = w; item < nlast * p.R; item += nw)
+        merge_unit_head(p, last[1 + item / p.R].di, item % p.R);
 }
 
 }  // namespace hpc

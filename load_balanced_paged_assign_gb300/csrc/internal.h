@@ -14,6 +14,7 @@ namespace hpc {
 constexpr int kHeadDim = 128;
 constexpr int kTile = 64;  // tokens per tile = tokens per page
 constexpr int kMaxGroup = 8;
+constexpr int kMaxRows = 16;  // query rows of one KV head in a descriptor: q_len * G
 constexpr int kConsumerWarps = 4;  // consumer warps per tile of a stage
 constexpr int kPlanThreads = 1024;
 
@@ -41,24 +42,27 @@ struct AttnParams {
     int min_tiles;     // floor the map was planned with (load-balanced maps)
     int fly;           // 1: derive the first descriptor from the seqlens (load-balanced maps)
     int B, Hq, Hkv, G, max_pages, num_pages;
+    int q_len;  // query tokens per request (the last q_len live tokens; causal among them)
+    int R;      // query rows per KV head: q_len * G (row rho = i * G + g)
     float score_scale;  // sm_scale * log2(e), times k_scale for FP8
     float v_scale;      // 1 for BF16
 };
 
-// Attention kernel configuration for one KV dtype.
+// Attention kernel configuration for one KV dtype and row-block count nb
+// (query rows per KV head R <= 8 nb; nb = 1 or 2).
 struct AttnConfig {
     const void *kernel;
     int smem_bytes;
     int threads;
 };
 
-AttnConfig attn_config_bf16();
-AttnConfig attn_config_fp8();
+AttnConfig attn_config_bf16(int nb);
+AttnConfig attn_config_fp8(int nb);
 
-cudaError_t launch_attn_bf16(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                             int grid, cudaStream_t s);
-cudaError_t launch_attn_fp8(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                            int grid, cudaStream_t s);
+cudaError_t launch_attn_bf16(int nb, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_attn_fp8(int nb, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const AttnParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages, int num_ctas,
                           int floor, const hpc_task_map &map, cudaStream_t s);
@@ -67,6 +71,6 @@ cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_p
 int assign_smem_bytes(int B);
 
 cudaError_t launch_combine(const float *part_o, const float *part_lse, const hpc_task_map &map,
-                           int B, int Hq, int Hkv, void *out, cudaStream_t s);
+                           int B, int Hq, int Hkv, int q_len, void *out, cudaStream_t s);
 
 }  // namespace hpc

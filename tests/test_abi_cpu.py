@@ -184,3 +184,25 @@ def test_rope_norm_argument_checks(hd):
     assert L.hpc_rope_frequencies(0.0, FAKE, None) == E.HPC_ERR_ARG
     assert L.hpc_rope_frequencies(1e4, None, None) == E.HPC_ERR_ARG
     assert L.hpc_rope_frequencies(1e4, FAKE + 8, None) == E.HPC_ERR_ARG
+
+
+def test_multi_query_argument_checks(hd):
+    m = fake_map(hd)
+    m.B, m.Hkv, m.num_ctas = 4, 1, 132
+    L = hd.lib()
+    E = hd.binding
+
+    def attn(q_len, Hq=8, Hkv=1):
+        return L.hpc_decode_attn_mq(FAKE, None, FAKE, FAKE, 10, 1.0, 1.0, 0, FAKE, 4, FAKE, 4,
+                                    Hq, Hkv, 128, q_len, 0.088, ctypes.byref(m), FAKE, FAKE, None)
+
+    assert attn(0) == E.HPC_ERR_ARG
+    assert attn(3) == E.HPC_ERR_UNSUPPORTED  # 3 x 8 = 24 query rows per KV head > 16
+    assert attn(17, Hq=1) == E.HPC_ERR_UNSUPPORTED
+    assert L.hpc_decode_combine_mq(FAKE, FAKE, ctypes.byref(m), 4, 8, 1, 128, 0, FAKE,
+                                   None) == E.HPC_ERR_ARG
+    assert L.hpc_decode_combine_mq(FAKE, FAKE, ctypes.byref(m), 4, 8, 1, 128, 3, FAKE,
+                                   None) == E.HPC_ERR_UNSUPPORTED
+    assert L.hpc_decode_step_mq(FAKE, None, FAKE, FAKE, 10, 1.0, 1.0, 0, FAKE, 4, FAKE, 4, 8, 1,
+                                128, 4, 0.088, 132, 2, 0, ctypes.byref(m), FAKE, FAKE, FAKE, FAKE,
+                                None) == E.HPC_ERR_UNSUPPORTED
