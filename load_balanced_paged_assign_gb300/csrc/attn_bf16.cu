@@ -19,12 +19,16 @@ using TraitsBf16 = AttnTraits<false, kStagesBf16, kTpsBf16, 1>;
 #ifndef HPC_BF16_STAGES_MQ
 #define HPC_BF16_STAGES_MQ 3
 #endif
+#ifndef HPC_BF16_TPS_MQ
+#define HPC_BF16_TPS_MQ 1
+#endif
 constexpr int kStagesBf16Mq = HPC_BF16_STAGES_MQ;
-using TraitsBf16Mq = AttnTraits<false, kStagesBf16Mq, 1, 2>;
+constexpr int kTpsBf16Mq = HPC_BF16_TPS_MQ;
+using TraitsBf16Mq = AttnTraits<false, kStagesBf16Mq, kTpsBf16Mq, 2>;
 
 AttnConfig attn_config_bf16(int nb) {
     if (nb == 2)
-        return {reinterpret_cast<const void *>(&attn_kernel<false, kStagesBf16Mq, 1, 2>),
+        return {reinterpret_cast<const void *>(&attn_kernel<false, kStagesBf16Mq, kTpsBf16Mq, 2>),
                 TraitsBf16Mq::kSmemBytes, TraitsBf16Mq::kThreads};
     return {reinterpret_cast<const void *>(&attn_kernel<false, kStagesBf16, kTpsBf16, 1>),
             TraitsBf16::kSmemBytes, TraitsBf16::kThreads};
@@ -45,7 +49,7 @@ cudaError_t launch_attn_bf16(int nb, const CUtensorMap &tk, const CUtensorMap &t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (nb == 2) return cudaLaunchKernelEx(&cfg, attn_kernel<false, kStagesBf16Mq, 1, 2>, tk, tv, p);
+    if (nb == 2) return cudaLaunchKernelEx(&cfg, attn_kernel<false, kStagesBf16Mq, kTpsBf16Mq, 2>, tk, tv, p);
     return cudaLaunchKernelEx(&cfg, attn_kernel<false, kStagesBf16, kTpsBf16, 1>, tk, tv, p);
 }
 

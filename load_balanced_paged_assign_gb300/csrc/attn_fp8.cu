@@ -15,17 +15,21 @@ constexpr int kStagesFp8 = HPC_FP8_STAGES;  // pipeline depth (build-time tunabl
 constexpr int kTpsFp8 = HPC_FP8_TPS;        // tiles per stage: 1 or 2
 using TraitsFp8 = AttnTraits<true, kStagesFp8, kTpsFp8, 1>;
 // Multi-query decode with 8 < q_len * G <= 16 query rows per KV head: twice
-// the state per consumer, so fewer consumers per stage (one tile) and the
-// ring sized to the remaining shared memory.
+// the state per consumer; eight consumers (two tiles per stage) hide the
+// per-tile latency as in decode, with a single hand-off slot to fit.
 #ifndef HPC_FP8_STAGES_MQ
-#define HPC_FP8_STAGES_MQ 6
+#define HPC_FP8_STAGES_MQ 4
+#endif
+#ifndef HPC_FP8_TPS_MQ
+#define HPC_FP8_TPS_MQ 2
 #endif
 constexpr int kStagesFp8Mq = HPC_FP8_STAGES_MQ;
-using TraitsFp8Mq = AttnTraits<true, kStagesFp8Mq, 1, 2>;
+constexpr int kTpsFp8Mq = HPC_FP8_TPS_MQ;
+using TraitsFp8Mq = AttnTraits<true, kStagesFp8Mq, kTpsFp8Mq, 2>;
 
 AttnConfig attn_config_fp8(int nb) {
     if (nb == 2)
-        return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8Mq, 1, 2>),
+        return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8Mq, kTpsFp8Mq, 2>),
                 TraitsFp8Mq::kSmemBytes, TraitsFp8Mq::kThreads};
     return {reinterpret_cast<const void *>(&attn_kernel<true, kStagesFp8, kTpsFp8, 1>),
             TraitsFp8::kSmemBytes, TraitsFp8::kThreads};
@@ -46,7 +50,7 @@ cudaError_t launch_attn_fp8(int nb, const CUtensorMap &tk, const CUtensorMap &tv
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (nb == 2) return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8Mq, 1, 2>, tk, tv, p);
+    if (nb == 2) return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8Mq, kTpsFp8Mq, 2>, tk, tv, p);
     return cudaLaunchKernelEx(&cfg, attn_kernel<true, kStagesFp8, kTpsFp8, 1>, tk, tv, p);
 }
 

@@ -83,7 +83,6 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFullMask = 0xffffffffu;
-constexpr int kCombSlots = 2;   // hand-off slots (double buffer)
 constexpr int kStateRegs = 36;  // per lane and row block: 32 accumulators, m0, m1, l0, l1
 constexpr int kMaxLast = 16;    // split units whose merge this CTA owes, held at once
 constexpr int kStageStride = kHeadDim + 4;  // floats per head row of the combiner's staging
@@ -112,17 +111,20 @@ struct AttnTraits {
     static constexpr int kQBytes = kRows * kHeadDim * kElem;        // Q slot per stage
     static constexpr int kState = kStateRegs * NB;                   // state floats per lane
     static constexpr int kSlotFloats = kConsumers * kState * 32;     // one hand-off slot
+    // consumer -> combiner hand-off slots: double-buffered, except when two
+    // row blocks on eight consumers make a slot too large for two to fit
+    static constexpr int kSlots = NB * TPS >= 4 ? 1 : 2;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + STAGES * kStageKV;
     static constexpr int kOffQ = kOffV + STAGES * kStageKV;
     static constexpr int kOffInfo = kOffQ + STAGES * kQBytes;
     static constexpr int kOffComb = kOffInfo + STAGES * (int)sizeof(StageInfo);
-    static constexpr int kOffStage = kOffComb + kCombSlots * kSlotFloats * 4;
+    static constexpr int kOffStage = kOffComb + kSlots * kSlotFloats * 4;
     static constexpr int kOffSlotInfo = kOffStage + kRows * kStageStride * 4;
-    static constexpr int kOffLast = kOffSlotInfo + kCombSlots * (int)sizeof(SlotInfo);
+    static constexpr int kOffLast = kOffSlotInfo + kSlots * (int)sizeof(SlotInfo);
     static constexpr int kOffBar = kOffLast + (kMaxLast + 1) * (int)sizeof(SlotInfo);
     // full[STAGES], empty[STAGES], slot full[2], slot empty[2], end rendezvous
-    static constexpr int kNumBars = 2 * STAGES + 2 * kCombSlots + 1;
+    static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // abort word
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;  // slack to align the base to 1024 B
@@ -464,13 +466,13 @@ __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem
     const SlotInfo *slots = reinterpret_cast<const SlotInfo *>(smem + Tr::kOffSlotInfo);
     SlotInfo *last = reinterpret_cast<SlotInfo *>(smem + Tr::kOffLast);  // [0].flags = count
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
-    uint64_t *slot_full = bars + 2 * STAGES, *slot_empty = slot_full + kCombSlots;
+    uint64_t *slot_full = bars + 2 * STAGES, *slot_empty = slot_full + Tr::kSlots;
     const bool fused = p.out != nullptr;
     int nlast = 0;
 
     for (uint32_t n = 0;; ++n) {
-        const int k = n % kCombSlots;
-        if (!warp_wait(&slot_full[k], (n / kCombSlots) & 1u, abort)) return false;
+        const int k = n % Tr::kSlots;
+        if (!warp_wait(&slot_full[k], (n / Tr::kSlots) & 1u, abort)) return false;
         const SlotInfo si = slots[k];
         if (si.flags & kEnd) break;
         // [warp][lane][36 NB]: this lane's 9 NB float4 of every consumer warp;
@@ -596,7 +598,7 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
     const StageInfo *info = reinterpret_cast<const StageInfo *>(smem + Tr::kOffInfo);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Tr::kOffBar);
     uint64_t *empty = full + STAGES;
-    uint64_t *slot_full = full + 2 * STAGES, *slot_empty = slot_full + kCombSlots;
+    uint64_t *slot_full = full + 2 * STAGES, *slot_empty = slot_full + Tr::kSlots;
     float *comb = reinterpret_cast<float *>(smem + Tr::kOffComb);
     SlotInfo *slots = reinterpret_cast<SlotInfo *>(smem + Tr::kOffSlotInfo);
     const uint32_t sK0 = smem_u32(smem + Tr::kOffK) + slot * Tr::kTileBytes;
@@ -834,8 +836,8 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
         if (lane == 0 && !(flags & kEnd)) mbar_arrive(&empty[stage]);  // stage may be refilled
 
         if (flags & (kLast | kEnd)) {  // hand the state (or the end) to the combiner
-            const int k = handed % kCombSlots;
-            if (!warp_wait(&slot_empty[k], ((handed / kCombSlots) & 1u) ^ 1u, abort))
+            const int k = handed % Tr::kSlots;
+            if (!warp_wait(&slot_empty[k], ((handed / Tr::kSlots) & 1u) ^ 1u, abort))
                 return false;
             if (flags & kLast) {  // lane-major: 9 NB float4 per lane, conflict-free
                 float4 *dst = reinterpret_cast<float4 *>(
@@ -874,11 +876,11 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
             mbar_init(&bars[s], 1);                          // full: producer arrive + TMA bytes
             mbar_init(&bars[STAGES + s], Tr::kConsumers);    // empty: one arrive per consumer warp
         }
-        for (int k = 0; k < kCombSlots; ++k) {
+        for (int k = 0; k < Tr::kSlots; ++k) {
             mbar_init(&bars[2 * STAGES + k], 32 * Tr::kConsumers);   // slot full: every consumer lane
-            mbar_init(&bars[2 * STAGES + kCombSlots + k], 1);        // slot empty: the combiner
+            mbar_init(&bars[2 * STAGES + Tr::kSlots + k], 1);        // slot empty: the combiner
         }
-        mbar_init(&bars[2 * STAGES + 2 * kCombSlots], 32 * (Tr::kConsumers + 1));  // end rendezvous
+        mbar_init(&bars[2 * STAGES + 2 * Tr::kSlots], 32 * (Tr::kConsumers + 1));  // end rendezvous
         *abort = 0;
         fence_barrier_init();
     }
@@ -933,7 +935,7 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
     // End of the stream: the combiner has published the split units whose
     // merge this CTA owes; all non-producer warps merge them, one warp per
     // (unit, head).
-    uint64_t *end_bar = bars + 2 * STAGES + 2 * kCombSlots;
+    uint64_t *end_bar = bars + 2 * STAGES + 2 * Tr::kSlots;
     mbar_arrive(end_bar);
     if (!warp_wait(end_bar, 0, abort)) {
         grid_dependency_wait();
