@@ -332,3 +332,24 @@ def make_prologue_inputs(pw: PrologueWorkload, device="cpu", seed: int | None = 
     token_req = torch.zeros(N, dtype=torch.int32, device=device)
     return PrologueInputs(pw, qkv, wq, wk, positions, token_req, bt, k_cache, v_cache, k_scale,
                           v_scale)
+
+
+# ---------------------------------------------------------------- router GEMM
+# Inputs of the router GEMM (BF16 hidden states x FP32 router weights), at
+# the SGLang post's router shape: K = 4096 hidden, N = 192 experts, M tokens.
+# Recipe: X ~ N(0, 1) rounded to BF16 [M, K]; W ~ N(0, 1/K) in FP32 [N, K]
+# (a Linear layer's weight), so the scores are about N(0, 1).  The post's
+# sweep prints no M values; the workloads span decode (a few tokens) to
+# prefill (thousands).
+
+ROUTER_K, ROUTER_N = 4096, 192
+ROUTER_MS = (1, 16, 64, 256, 1024, 4096, 16384)
+
+
+def make_router_inputs(M: int, K: int = ROUTER_K, N: int = ROUTER_N, seed: int = 1300,
+                       device="cpu") -> tuple:
+    """(x bf16 [M, K], w fp32 [N, K]) per the recipe above."""
+    gen = torch.Generator().manual_seed(seed)
+    w = (torch.randn((N, K), generator=gen, dtype=torch.float32) / math.sqrt(K)).to(device)
+    x = _normal((M, K), seed + 1, device).to(torch.bfloat16)
+    return x, w
