@@ -467,6 +467,48 @@ hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride, const void *
                          void *d_q_out, float *d_q_scale_out, int32_t *d_flags,
                          const hpc_rope_norm_params *params, hpc_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Router GEMM with FP32 weights on BF16 tensor cores (SGLang post, section
+ * "Router GEMM：在路由精度与吞吐量之间取得平衡", and its summary bullet): the
+ * FP32 router weight W is split once into W_high, its BF16 truncation (low 16
+ * bits dropped), and W_low, the round-to-nearest BF16 of (W - W_high) * 256,
+ * so W ~ W_high + W_low / 256; the scores are
+ *     S = X W_high^T + (X W_low^T) / 256,
+ * both products accumulated in FP32 (tcgen05 tensor cores, TMEM
+ * accumulators), the 1/256 applied in the epilogue.  The split keeps every
+ * weight within 2^-16 of its magnitude.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Splits d_w (device fp32 [N, K], row-major: experts x hidden, a Linear
+ * layer's weight) into d_w_hi and d_w_lo (device bf16 [N, K]).  Done once,
+ * when the weights are loaded.  Asynchronous on `stream`.
+ */
+hpc_status hpc_router_split(const float *d_w, int32_t N, int32_t K, void *d_w_hi, void *d_w_lo,
+                            hpc_stream_t stream);
+
+/*
+ * Bytes of the fp32 workspace hpc_router_gemm uses on the current device for
+ * this shape (split-K partials when tokens are few); 0 when it needs none,
+ * -1 for a shape it does not support.
+ */
+int64_t hpc_router_workspace_bytes(int32_t M, int32_t N, int32_t K);
+
+/*
+ * S = X W_high^T + (X W_low^T) / 256 for d_x (device bf16 [M, K], row-major
+ * tokens x hidden) into d_out (device fp32 [M, N]).  K must be a multiple of
+ * 64 and N of 16 (HPC_ERR_UNSUPPORTED otherwise); all pointers 16-byte
+ * aligned.  d_workspace (hpc_router_workspace_bytes bytes, or less: the call
+ * then uses fewer K splits, down to none) holds split-K partials, which a
+ * second kernel sums in a fixed order, so the result is deterministic.
+ * d_flags (device int32 or NULL) gets HPC_FLAG_TIMEOUT if a pipeline wait
+ * timed out (output invalid).  Asynchronous on `stream`; reads X only after
+ * the previous kernel on the stream has finished.
+ */
+hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const void *d_w_lo, int32_t M,
+                           int32_t N, int32_t K, float *d_out, void *d_workspace,
+                           int64_t workspace_bytes, int32_t *d_flags, hpc_stream_t stream);
+
 /*
  * Synchronises `stream` and copies map->meta into host_meta[4]
  * ({total_tiles, budget, num_desc, error_flags}).

@@ -16,6 +16,7 @@ from .binding import (EXPORTS, HPC_KV_BF16, HPC_KV_FP8_E4M3, HPC_ROPE_HALVES,
                       hpc_decode_read_meta, hpc_decode_static_capacity, hpc_decode_step,
                       hpc_decode_step_mq,
                       hpc_decode_step_host, hpc_decode_version, hpc_rope_frequencies, hpc_rope_norm,
+                      hpc_router_gemm, hpc_router_split, hpc_router_workspace_bytes,
                       kv_dtype_of, lib)
 
 __all__ = [
@@ -25,5 +26,6 @@ __all__ = [
     "hpc_decode_combine_mq", "hpc_decode_desc_capacity", "hpc_decode_num_ctas",
     "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_read_meta",
     "hpc_decode_static_capacity", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_step_mq",
-    "hpc_decode_version", "hpc_rope_frequencies", "hpc_rope_norm", "kv_dtype_of", "lib",
+    "hpc_decode_version", "hpc_rope_frequencies", "hpc_rope_norm", "hpc_router_gemm",
+    "hpc_router_split", "hpc_router_workspace_bytes", "kv_dtype_of", "lib",
 ]

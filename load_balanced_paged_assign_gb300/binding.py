@@ -28,6 +28,7 @@ EXPORTS = (
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
     "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
     "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
+    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_gemm",
 )
 
 
@@ -101,6 +102,9 @@ def lib():
                                                    vp, i32, vp, i32, i32, i32, i32, f32, i32, i32,
                                                    vp, vp, vp]),
         "hpc_rope_frequencies": (ctypes.c_int, [f32, vp, vp]),
+        "hpc_router_split": (ctypes.c_int, [vp, i32, i32, vp, vp, vp]),
+        "hpc_router_workspace_bytes": (i64, [i32, i32, i32]),
+        "hpc_router_gemm": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
         "hpc_decode_attn_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp,
                                               i32, vp, i32, i32, i32, i32, i32, f32, tm, vp, vp,
                                               vp]),
@@ -311,6 +315,27 @@ def hpc_decode_step_mq(q, q_scale, k_cache, v_cache, k_scale, v_scale, block_tab
         HEAD_DIM, int(q_len), float(sm_scale), int(num_ctas), int(min_tiles_per_cta),
         int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(unit_done),
         _ptr(out), _stream(stream)))
+
+
+def hpc_router_split(w, w_hi, w_lo, stream=None):
+    """Split fp32 router weights [N, K] into BF16 W_high / W_low [N, K]."""
+    N, K = w.shape
+    _check("hpc_router_split", lib().hpc_router_split(_ptr(w), int(N), int(K), _ptr(w_hi),
+                                                        _ptr(w_lo), _stream(stream)))
+
+
+def hpc_router_workspace_bytes(M, N, K) -> int:
+    return int(lib().hpc_router_workspace_bytes(int(M), int(N), int(K)))
+
+
+def hpc_router_gemm(x, w_hi, w_lo, out, workspace=None, flags=None, stream=None):
+    """Router scores out [M, N] fp32 = X W_high^T + (X W_low^T) / 256."""
+    M, K = x.shape
+    N = w_hi.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("hpc_router_gemm", lib().hpc_router_gemm(
+        _ptr(x), _ptr(w_hi), _ptr(w_lo), int(M), int(N), int(K), _ptr(out), _ptr(workspace),
+        int(ws_bytes), _ptr(flags), _stream(stream)))
 
 
 def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d_q_scale,

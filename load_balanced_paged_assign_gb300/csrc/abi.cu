@@ -256,6 +256,10 @@ hpc_status combine_impl(const float *d_part_o, const float *d_part_lse, const hp
 
 }  // namespace
 
+namespace hpc {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encoder(); }
+}  // namespace hpc
+
 extern "C" {
 
 const char *hpc_decode_version(void) { return "hpc_decode 0.1 (sm_103a)"; }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -69,6 +70,9 @@ cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages,
 cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_pages,
                                int num_splits, const hpc_task_map &map, cudaStream_t s);
 int assign_smem_bytes(int B);
+
+// cuTensorMapEncodeTiled from the driver (nullptr when unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_combine(const float *part_o, const float *part_lse, const hpc_task_map &map,
                            int B, int Hq, int Hkv, int q_len, void *out, cudaStream_t s);

@@ -206,3 +206,23 @@ def test_multi_query_argument_checks(hd):
     assert L.hpc_decode_step_mq(FAKE, None, FAKE, FAKE, 10, 1.0, 1.0, 0, FAKE, 4, FAKE, 4, 8, 1,
                                 128, 4, 0.088, 132, 2, 0, ctypes.byref(m), FAKE, FAKE, FAKE, FAKE,
                                 None) == E.HPC_ERR_UNSUPPORTED
+
+
+def test_router_argument_checks(hd):
+    L = hd.lib()
+    E = hd.binding
+    assert L.hpc_router_gemm(FAKE, FAKE, FAKE, 0, 192, 4096, FAKE, None, 0, None, None) == E.HPC_OK
+    assert L.hpc_router_gemm(FAKE, FAKE, FAKE, 4, 192, 4000, FAKE, None, 0, None, None) == \
+        E.HPC_ERR_UNSUPPORTED  # K not a multiple of 64
+    assert L.hpc_router_gemm(FAKE, FAKE, FAKE, 4, 190, 4096, FAKE, None, 0, None, None) == \
+        E.HPC_ERR_UNSUPPORTED  # N not a multiple of 16
+    assert L.hpc_router_gemm(None, FAKE, FAKE, 4, 192, 4096, FAKE, None, 0, None, None) == \
+        E.HPC_ERR_ARG
+    assert L.hpc_router_gemm(FAKE + 8, FAKE, FAKE, 4, 192, 4096, FAKE, None, 0, None, None) == \
+        E.HPC_ERR_ARG
+    assert L.hpc_router_gemm(FAKE, FAKE, FAKE, -1, 192, 4096, FAKE, None, 0, None, None) == \
+        E.HPC_ERR_ARG
+    assert L.hpc_router_split(None, 192, 4096, FAKE, FAKE, None) == E.HPC_ERR_ARG
+    assert L.hpc_router_split(FAKE, 0, 4096, FAKE, FAKE, None) == E.HPC_ERR_ARG
+    assert L.hpc_router_workspace_bytes(4, 192, 4000) == -1
+    assert L.hpc_router_workspace_bytes(0, 192, 4096) == 0
