@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024  # twice the GB300 L2
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "decode-attn µs/step and achieved HBM GB/s (% of GB300 peak) on mixed-length batches"
 
 
@@ -91,6 +92,24 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense BF16 tensor peak (burst, for a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def router_cost(M, N, K, splits):
+    """FLOPs (two BF16 products) and algorithmic bytes of one router GEMM:
+    X once, W_high and W_low once, the scores written, plus the split-K
+    partials written and read back when the K range is split."""
+    flops = 2 * 2 * M * N * K
+    nbytes = M * K * 2 + 2 * N * K * 2 + M * N * 4 + (2 * splits * M * N * 4 if splits > 1 else 0)
+    return flops, nbytes
 
 
 def profiled_traffic(kernel_src_hash, kv_dtype, workload):
@@ -236,6 +255,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue", action="store_true")
     ap.add_argument("--no-mtp", action="store_true")
+    ap.add_argument("--no-router", action="store_true")
     ap.add_argument("--floor", type=int, default=None)
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
@@ -605,6 +625,46 @@ def main():
                "speedup_vs_two_decode_steps": 2 * mean_step / mtp_us}
         del b2, ws2
 
+    # ---- router GEMM (BF16 hi/lo split of FP32 weights, tcgen05) over the
+    # token sweep at the post's shape; cuBLAS FP32 / TF32 timed beside it as
+    # the post's own comparison points (context, not part of the path)
+    router = None
+    if not args.no_router:
+        from load_balanced_paged_assign_gb300.workloads import (ROUTER_K, ROUTER_MS, ROUTER_N,
+                                                                make_router_inputs)
+        tf_peak, tf_kind = measured_bf16_tflops()
+        rows = []
+        n_r = min(args.steps, 200)
+        for M in ROUTER_MS:
+            x, wr = make_router_inputs(M, device=dev)
+            hi = torch.empty((ROUTER_N, ROUTER_K), dtype=torch.bfloat16, device=dev)
+            lo = torch.empty_like(hi)
+            hd.hpc_router_split(wr, hi, lo)
+            out_r = torch.empty((M, ROUTER_N), device=dev)
+            nbw = hd.hpc_router_workspace_bytes(M, ROUTER_N, ROUTER_K)
+            ws_r = torch.empty(max(nbw // 4, 1), device=dev) if nbw > 0 else None
+            splits = nbw // (M * ROUTER_N * 4) if nbw > 0 else 1
+            us = statistics.fmean(timed(n_r, args.warmup,
+                                        lambda: hd.hpc_router_gemm(x, hi, lo, out_r, ws_r)))
+            xf, wt = x.float(), wr.t().contiguous()
+            torch.backends.cuda.matmul.allow_tf32 = False
+            fp32_us = statistics.fmean(timed(n_r, args.warmup, lambda: torch.matmul(xf, wt)))
+            torch.backends.cuda.matmul.allow_tf32 = True
+            tf32_us = statistics.fmean(timed(n_r, args.warmup, lambda: torch.matmul(xf, wt)))
+            torch.backends.cuda.matmul.allow_tf32 = False
+            flops, nb = router_cost(M, ROUTER_N, ROUTER_K, splits)
+            tflops, gbs = flops / (us * 1e-6) / 1e12, nb / (us * 1e-6) / 1e9
+            bound = "tensor" if tflops / tf_peak > gbs / peak else "hbm"
+            rows.append({"M": M, "us": us, "splits": splits, "tflops": tflops, "gbps": gbs,
+                         "bound": bound,
+                         "frac": tflops / tf_peak if bound == "tensor" else gbs / peak,
+                         "cublas_fp32_us": fp32_us, "cublas_tf32_us": tf32_us,
+                         "speedup_vs_fp32": fp32_us / us, "speedup_vs_tf32": tf32_us / us})
+            del x, wr, hi, lo, out_r, ws_r, xf, wt
+        router = {"K": ROUTER_K, "N": ROUTER_N, "peaks": {"bf16_tflops": tf_peak,
+                                                          "hbm_gbs": peak, "kind": tf_kind},
+                  "sweep": rows}
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
@@ -638,6 +698,7 @@ def main():
         "static": static,
         "rope_norm": prologue,
         "mtp": mtp,
+        "router_gemm": router,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }

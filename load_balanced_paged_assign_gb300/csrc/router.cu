@@ -18,8 +18,10 @@
 //   * warps 2-5 wait for the last commit, read both accumulators with
 //     tcgen05.ld (warp w reads TMEM lanes 32 (w mod 4) ..), and write
 //     hi + lo / 256 (exact scaling) as FP32 scores, or as a split's partial;
-//   * with split-K a second kernel sums the partials in split order, so the
-//     result is deterministic.
+//   * with split-K a second kernel sums the partials in a fixed order, so the
+//     result is deterministic;
+//   * up to 16 tokens the product is a weight-bound matrix-vector product:
+//     a CUDA-core kernel reads the split weights once with no split-K pass.
 // Every mbarrier wait is bounded; on a timeout the CTA raises the error
 // flag, waits (bounded) for its copies in flight, frees its TMEM and leaves.
 #include <cuda_bf16.h>
@@ -200,21 +202,164 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// out[i] = sum over splits s of partials[s][i], in split order.
-__global__ void router_reduce_kernel(const float4 *__restrict__ partials, float4 *__restrict__ out,
-                                     size_t n4, int splits) {
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// out[i] = sum over at most 8 splits, in split order: one thread per float4,
+// its loads all in flight together.
+__global__ void __launch_bounds__(256)
+    router_reduce_few_kernel(const float4 *__restrict__ partials, float4 *__restrict__ out,
+                             size_t n4, int splits) {
     grid_dependency_wait();
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-         i += (size_t)gridDim.x * blockDim.x) {
-        float4 acc = partials[i];
-        for (int s = 1; s < splits; ++s) {
-            const float4 v = partials[(size_t)s * n4 + i];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        v[c] = c < splits ? __ldcg(partials + (size_t)c * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = v[0];
+#pragma unroll
+    for (int c = 1; c < 8; ++c) acc = add4(acc, v[c]);
+    out[i] = acc;
+}
+
+// out[i] = sum over splits s of partials[s][i] (more than 8).  A block takes 32 float4s;
+// its eight warp-rows of threads g = 0..7 each sum the splits s = g mod 8
+// (all their loads in flight together), and the eight sums are combined in
+// the order g = 0..7 through shared memory, so the result does not depend on
+// timing.
+__global__ void __launch_bounds__(256)
+    router_reduce_kernel(const float4 *__restrict__ partials, float4 *__restrict__ out,
+                         size_t n4, int splits) {
+    __shared__ float4 part[8][32];
+    grid_dependency_wait();
+    const int e = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const size_t i = (size_t)blockIdx.x * 32 + e;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < n4) {
+        float4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int sp = g + 8 * c;
+            v[c] = sp < splits ? __ldcg(partials + (size_t)sp * n4 + i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        out[i] = acc;
+        for (int sp = g + 64; sp < splits; sp += 8) acc = add4(acc, __ldcg(partials + (size_t)sp * n4 + i));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc = add4(acc, v[c]);
+    }
+    part[g][e] = acc;
+    __syncthreads();
+    if (g == 0 && i < n4) {
+        float4 sum = part[0][e];
+#pragma unroll
+        for (int c = 1; c < 8; ++c) sum = add4(sum, part[c][e]);
+        out[i] = sum;
+    }
+}
+
+// Few tokens (M <= kGemvMaxM): the product is bound by reading the split
+// weights (2 N K BF16), so CUDA cores do it with no split-K pass.  A CTA owns
+// kGemvExperts experts over the whole K and one 256-thread group per eight
+// tokens (the groups read the same weights, the second time from L1); in a
+// group, warp w takes every eighth 256-wide K block and a lane 8 consecutive
+// K.  Both products are accumulated separately in FP32 (as the method
+// states) and reduced in a fixed order: lanes by shuffles, then warps 0..7
+// through shared memory.
+constexpr int kGemvMaxM = 16;
+constexpr int kGemvExperts = 2;
+constexpr int kGemvRows = 8;  // tokens per 256-thread group at most
+
+__device__ __forceinline__ void bf16x8(uint4 v, float (&f)[8]) {
+    f[0] = bf16lo_to_f32(v.x), f[1] = bf16hi_to_f32(v.x);
+    f[2] = bf16lo_to_f32(v.y), f[3] = bf16hi_to_f32(v.y);
+    f[4] = bf16lo_to_f32(v.z), f[5] = bf16hi_to_f32(v.z);
+    f[6] = bf16lo_to_f32(v.w), f[7] = bf16hi_to_f32(v.w);
+}
+
+template <int MM>  // tokens per group (M <= MM * groups)
+__global__ void __launch_bounds__(256 * (kGemvMaxM / kGemvRows))
+    router_gemv_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ whi,
+                       const uint4 *__restrict__ wlo, float *__restrict__ out, int M, int N,
+                       int K) {
+    __shared__ float red[kGemvMaxM / kGemvRows][8][MM][kGemvExperts][2];
+    grid_dependency_wait();
+    const int grp = threadIdx.x >> 8, tid = threadIdx.x & 255;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int m0 = grp * MM;
+    const int n0 = blockIdx.x * kGemvExperts;
+    const int K8 = K / 8;  // 16-byte vectors per row
+    float acc[MM][kGemvExperts][2];
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+        for (int e = 0; e < kGemvExperts; ++e) acc[m][e][0] = acc[m][e][1] = 0.f;
+    // U K vectors per step, all their loads issued before any use (U = 2 when
+    // the registers allow: twice the bytes in flight per thread)
+    constexpr int U = MM <= 4 ? 2 : 1;
+    for (int v0 = warp * 32 + lane; v0 < K8; v0 += 256 * U) {
+        uint4 wv[U][kGemvExperts][2], xp[U][MM];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 256 * u;
+            const bool in = v < K8;
+#pragma unroll
+            for (int e = 0; e < kGemvExperts; ++e) {
+                const int n = min(n0 + e, N - 1);
+                wv[u][e][0] = in ? __ldg(whi + (size_t)n * K8 + v) : make_uint4(0u, 0u, 0u, 0u);
+                wv[u][e][1] = in ? __ldg(wlo + (size_t)n * K8 + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int m = 0; m < MM; ++m)
+                xp[u][m] = in && m0 + m < M ? __ldg(x + (size_t)(m0 + m) * K8 + v)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float h[kGemvExperts][8], l[kGemvExperts][8];
+#pragma unroll
+            for (int e = 0; e < kGemvExperts; ++e) {
+                bf16x8(wv[u][e][0], h[e]);
+                bf16x8(wv[u][e][1], l[e]);
+            }
+#pragma unroll
+            for (int m = 0; m < MM; ++m) {
+                float xv[8];
+                bf16x8(xp[u][m], xv);
+#pragma unroll
+                for (int e = 0; e < kGemvExperts; ++e)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc[m][e][0] = fmaf(xv[j], h[e][j], acc[m][e][0]);
+                        acc[m][e][1] = fmaf(xv[j], l[e][j], acc[m][e][1]);
+                    }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+        for (int e = 0; e < kGemvExperts; ++e)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                float t = acc[m][e][p];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) red[grp][warp][m][e][p] = t;
+            }
+    __syncthreads();
+    if (tid < MM * kGemvExperts) {
+        const int m = tid / kGemvExperts, e = tid - m * kGemvExperts;
+        if (m0 + m < M && n0 + e < N) {
+            float hi = 0.f, lo = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                hi += red[grp][w][m][e][0];
+                lo += red[grp][w][m][e][1];
+            }
+            out[(size_t)(m0 + m) * N + n0 + e] = hi + lo * (1.0f / 256.0f);
+        }
     }
 }
 
@@ -232,6 +377,32 @@ __global__ void router_split_kernel(const float *__restrict__ w, size_t n,
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+hpc_status cuda_status_of(cudaError_t e) { return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA; }
+
+template <int MM>
+cudaError_t launch_gemv_m(const void *x, const void *hi, const void *lo, float *out, int M, int N,
+                          int K, cudaStream_t s) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + kGemvExperts - 1) / kGemvExperts);
+    cfg.blockDim = dim3(256 * ((M + MM - 1) / MM));  // one group per MM tokens
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_gemv_kernel<MM>, static_cast<const uint4 *>(x),
+                              static_cast<const uint4 *>(hi), static_cast<const uint4 *>(lo),
+                              out, M, N, K);
+}
+
+cudaError_t launch_gemv(const void *x, const void *hi, const void *lo, float *out, int M, int N,
+                        int K, cudaStream_t s) {
+    if (M <= 1) return launch_gemv_m<1>(x, hi, lo, out, M, N, K, s);
+    if (M <= 4) return launch_gemv_m<4>(x, hi, lo, out, M, N, K, s);
+    return launch_gemv_m<kGemvRows>(x, hi, lo, out, M, N, K, s);  // 8 tokens per group
+}
 
 std::mutex g_mu;
 int g_smem_set[64];  // dynamic shared memory already allowed, per device
@@ -287,6 +458,7 @@ extern "C" hpc_status hpc_router_split(const float *d_w, int32_t N, int32_t K, v
 
 extern "C" int64_t hpc_router_workspace_bytes(int32_t M, int32_t N, int32_t K) {
     if (M < 0 || N <= 0 || K <= 0 || K % kBK || N % 16 || M == 0) return M == 0 ? 0 : -1;
+    if (M <= kGemvMaxM) return 0;  // the few-token path needs no partials
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     const Plan p = plan_for(M, N, K, sm_count(dev));
@@ -305,6 +477,8 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
     if (!d_x || !d_w_hi || !d_w_lo || !d_out) return HPC_ERR_ARG;
     if (!aligned16(d_x) || !aligned16(d_w_hi) || !aligned16(d_w_lo) || !aligned16(d_out))
         return HPC_ERR_ARG;
+    if (M <= kGemvMaxM) return cuda_status_of(launch_gemv(d_x, d_w_hi, d_w_lo, d_out, M, N, K,
+                                                          static_cast<cudaStream_t>(stream)));
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HPC_ERR_CUDA;
     Plan p = plan_for(M, N, K, sm_count(dev));
@@ -388,13 +562,14 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
     cudaError_t e = cudaLaunchKernelEx(&cfg, router_gemm_kernel, tx, thi, tlo, a);
     if (e == cudaSuccess && p.splits > 1) {
         const size_t n4 = (size_t)M * N / 4;
+        const bool few = p.splits <= 8;
         cudaLaunchConfig_t rc = {};
-        rc.gridDim = dim3((unsigned)std::min<size_t>((n4 + 255) / 256, 4096));
+        rc.gridDim = dim3((unsigned)(few ? (n4 + 255) / 256 : (n4 + 31) / 32));
         rc.blockDim = dim3(256);
         rc.stream = s;
         rc.attrs = attr;
         rc.numAttrs = 1;
-        e = cudaLaunchKernelEx(&rc, router_reduce_kernel,
+        e = cudaLaunchKernelEx(&rc, few ? router_reduce_few_kernel : router_reduce_kernel,
                                reinterpret_cast<const float4 *>(d_workspace),
                                reinterpret_cast<float4 *>(d_out), n4, p.splits);
     }
