@@ -14,10 +14,10 @@ constexpr int kStagesBf16 = HPC_BF16_STAGES;  // pipeline depth (build-time tuna
 constexpr int kTpsBf16 = HPC_BF16_TPS;        // tiles per stage: 1 or 2
 using TraitsBf16 = AttnTraits<false, kStagesBf16, kTpsBf16, 1>;
 // Multi-query decode with 8 < q_len * G <= 16 query rows per KV head: twice
-// the state per consumer, so fewer consumers per stage (one tile) and the
-// ring sized to the remaining shared memory.
+// the state per consumer; one tile per stage (four consumers), four stages
+// and a single consumer -> combiner hand-off slot to fit.
 #ifndef HPC_BF16_STAGES_MQ
-#define HPC_BF16_STAGES_MQ 3
+#define HPC_BF16_STAGES_MQ 4  // with one hand-off slot (measured faster than 3 with two)
 #endif
 #ifndef HPC_BF16_TPS_MQ
 #define HPC_BF16_TPS_MQ 1

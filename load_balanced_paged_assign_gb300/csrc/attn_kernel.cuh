@@ -111,9 +111,16 @@ struct AttnTraits {
     static constexpr int kQBytes = kRows * kHeadDim * kElem;        // Q slot per stage
     static constexpr int kState = kStateRegs * NB;                   // state floats per lane
     static constexpr int kSlotFloats = kConsumers * kState * 32;     // one hand-off slot
-    // consumer -> combiner hand-off slots: double-buffered, except when two
-    // row blocks on eight consumers make a slot too large for two to fit
-    static constexpr int kSlots = NB * TPS >= 4 ? 1 : 2;
+    // Shared memory of the layout below with `slots` hand-off slots.
+    static constexpr int bytes_with(int slots) {
+        return 2 * STAGES * kStageKV + STAGES * kQBytes + STAGES * (int)sizeof(StageInfo) +
+               slots * kSlotFloats * 4 + kRows * kStageStride * 4 +
+               slots * (int)sizeof(SlotInfo) + (kMaxLast + 1) * (int)sizeof(SlotInfo) +
+               (2 * STAGES + 2 * slots + 1) * 8 + 16 + 1024;
+    }
+    // consumer -> combiner hand-off slots: double-buffered when that fits
+    // (two row blocks double the state a slot holds)
+    static constexpr int kSlots = bytes_with(2) <= 227 * 1024 ? 2 : 1;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + STAGES * kStageKV;
     static constexpr int kOffQ = kOffV + STAGES * kStageKV;
