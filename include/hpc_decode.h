@@ -509,6 +509,34 @@ hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const void *d_w_
                            int32_t N, int32_t K, float *d_out, void *d_workspace,
                            int64_t workspace_bytes, int32_t *d_flags, hpc_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Extend / prefill attention (vLLM post, "Attention: HPC-Ops vs
+ * FlashAttention / Triton / FlashInfer", Table 4's prefill and extend rows):
+ * many new query tokens per request over the paged BF16 cache, on tcgen05
+ * tensor cores.  Request r holds L_r live tokens (d_seqlens, device); its
+ * last q_len tokens are the queries, already written into the cache, and
+ * query token i (position L_r - q_len + i) attends the tokens j <= L_r -
+ * q_len + i (causal).  A prefill is L_r = q_len; an extend has a cached
+ * prefix.  No task map: one CTA per (request, query head, 128 query tokens).
+ *   d_q        [B, q_len, Hq, 128] bf16, 16-byte aligned
+ *   caches     [num_pages, 64, Hkv, 128] bf16 (as for decode)
+ *   d_out      [B, q_len, Hq, 128] bf16, written for every query row; a row
+ *              that sees no token (L_r < q_len) is written as zeros
+ * Query head hq reads KV head hq / (Hq / Hkv); Hq % Hkv must be 0 and
+ * head_dim 128 (HPC_ERR_UNSUPPORTED otherwise).  d_flags (device int32 or
+ * NULL) gets HPC_FLAG_BAD_SEQLEN for a length outside [0, 64 *
+ * max_pages_per_req] (clamped), HPC_FLAG_BAD_PAGE for a page outside [0,
+ * num_pages) (not read; that request's output is invalid) and
+ * HPC_FLAG_TIMEOUT if a pipeline wait timed out.  Asynchronous on `stream`;
+ * reads its inputs only after the previous kernel on the stream has
+ * finished.  The caller owns all memory.
+ * ---------------------------------------------------------------------- */
+hpc_status hpc_prefill_attn(const void *d_q, const void *d_k_cache, const void *d_v_cache,
+                            int32_t num_pages, const int32_t *d_block_table,
+                            int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
+                            int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t q_len,
+                            float sm_scale, void *d_out, int32_t *d_flags, hpc_stream_t stream);
+
 /*
  * Synchronises `stream` and copies map->meta into host_meta[4]
  * ({total_tiles, budget, num_desc, error_flags}).

@@ -28,7 +28,7 @@ EXPORTS = (
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
     "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
     "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
-    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_gemm",
+    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_gemm", "hpc_prefill_attn",
 )
 
 
@@ -105,6 +105,8 @@ def lib():
         "hpc_router_split": (ctypes.c_int, [vp, i32, i32, vp, vp, vp]),
         "hpc_router_workspace_bytes": (i64, [i32, i32, i32]),
         "hpc_router_gemm": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
+        "hpc_prefill_attn": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
+                                            i32, f32, vp, vp, vp]),
         "hpc_decode_attn_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp,
                                               i32, vp, i32, i32, i32, i32, i32, f32, tm, vp, vp,
                                               vp]),
@@ -336,6 +338,16 @@ def hpc_router_gemm(x, w_hi, w_lo, out, workspace=None, flags=None, stream=None)
     _check("hpc_router_gemm", lib().hpc_router_gemm(
         _ptr(x), _ptr(w_hi), _ptr(w_lo), int(M), int(N), int(K), _ptr(out), _ptr(workspace),
         int(ws_bytes), _ptr(flags), _stream(stream)))
+
+
+def hpc_prefill_attn(q, k_cache, v_cache, block_table, seqlens, Hq, Hkv, q_len, sm_scale, out,
+                     flags=None, stream=None):
+    """Extend / prefill attention: q and out [B, q_len, Hq, 128] bf16, causal
+    over each request's last q_len live tokens."""
+    _check("hpc_prefill_attn", lib().hpc_prefill_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), _ptr(block_table),
+        int(block_table.shape[1]), _ptr(seqlens), int(seqlens.numel()), int(Hq), int(Hkv),
+        HEAD_DIM, int(q_len), float(sm_scale), _ptr(out), _ptr(flags), _stream(stream)))
 
 
 def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d_q_scale,

@@ -258,6 +258,10 @@ hpc_status combine_impl(const float *d_part_o, const float *d_part_lse, const hp
 
 namespace hpc {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encoder(); }
+hpc_status cache_tensor_map(CUtensorMap *m, const void *base, int32_t num_pages, int32_t Hkv,
+                            bool fp8) {
+    return make_cache_map(m, base, num_pages, Hkv, fp8);
+}
 }  // namespace hpc
 
 extern "C" {

@@ -74,6 +74,12 @@ int assign_smem_bytes(int B);
 // cuTensorMapEncodeTiled from the driver (nullptr when unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// TMA tensor map over one paged cache [num_pages, 64, Hkv, 128] (BF16: one
+// 64-dim half of one head's page per load, 128-byte swizzle; FP8: the whole
+// 128-byte rows of one head's page).
+hpc_status cache_tensor_map(CUtensorMap *m, const void *base, int32_t num_pages, int32_t Hkv,
+                            bool fp8);
+
 cudaError_t launch_combine(const float *part_o, const float *part_lse, const hpc_task_map &map,
                            int B, int Hq, int Hkv, int q_len, void *out, cudaStream_t s);
 

@@ -1,0 +1,532 @@
+// Extend / prefill attention over the paged BF16 KV cache on the fifth-
+// generation tensor cores: the "prefill" and "extend" rows of the vLLM
+// post's attention comparison (Table 4, "Attention: HPC-Ops vs
+// FlashAttention / Triton / FlashInfer").  Request r holds L_r live tokens in
+// its pages; the last q_len of them are the new query tokens, and query token
+// i (position L_r - q_len + i) attends every token at a position up to its
+// own (causal).  A prefill is the case L_r = q_len; an extend has a cached
+// prefix before the new tokens.
+//
+// GB300 design (tcgen05 + TMEM + TMA), one CTA per (request, query head,
+// block of 128 query tokens), heaviest (last) query blocks first:
+//   * warp 8 loads the CTA's Q tile once and then streams 128-token K and V
+//     tiles (two 64-token pages each, gathered through the block table) into
+//     two-stage rings with TMA (128-byte swizzle);
+//   * one thread of warp 9 issues tcgen05.mma: S_j = Q K_j^T into one of two
+//     TMEM score buffers, then O += P_{j-1} V_{j-1} into the TMEM output
+//     accumulator (V read as an MN-major operand straight from its cache
+//     layout), so the tensor cores compute the next scores while the softmax
+//     warps work on the current ones;
+//   * warps 0-7 run the online softmax, two warps per TMEM lane quarter (a
+//     row's 128 scores split into two halves of 64, their maxima exchanged
+//     through shared memory): they read S with tcgen05.ld, mask the causal
+//     diagonal, and write P = exp2(S * scale * log2 e - m) as BF16 into the
+//     shared-memory operand of the next PV product.  The running maximum m
+//     moves only when a tile's maximum exceeds it by more than 8 (log2
+//     units), so P stays <= 256 and the accumulator is rescaled (tcgen05.ld,
+//     multiply, tcgen05.st) only on those rare tiles; the result is the same
+//     softmax, since O and the row sum always share the reference m;
+//   * the epilogue divides O by the row sum and writes BF16.
+// Every mbarrier wait is bounded; on a timeout the CTA raises the error flag,
+// waits (bounded) for its copies and MMAs in flight, frees TMEM and leaves.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace hpc {
+namespace {
+
+constexpr int kQB = 128;                   // query rows per CTA (UMMA M)
+constexpr int kKB = 128;                   // KV tokens per tile
+constexpr int kHalf = 128 * 128;           // bytes of 128 rows x 64 BF16 (one 128-byte column block)
+constexpr int kTileBytes = 2 * kHalf;      // a 128 x 128 BF16 tile
+constexpr int kStages = 2;                 // K ring and V ring depth
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr uint32_t kTmemCols = 512;        // S0 [0, 128), S1 [128, 256), O [256, 384)
+constexpr int kOCol = 256;
+constexpr float kRescaleLog2 = 8.f;        // P <= 2^8 between reference moves
+
+// Shared-memory layout (offsets from the 1024-byte aligned base).
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffP = kOffV + kStages * kTileBytes;
+constexpr int kOffBar = kOffP + kTileBytes;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+// s_free[2], p_full, o_done, mma_done, xbar[4]
+constexpr int kNumBars = 1 + 2 * kStages * 2 + 2 + 2 + 3 + 4;
+constexpr int kOffX = kOffBar + kNumBars * 8;              // float [2][2][128] exchange
+constexpr int kOffMisc = kOffX + 2 * 2 * kQB * 4;          // tmem slot, abort word
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;           // + alignment slack
+
+struct PrefillArgs {
+    const int32_t *seqlens;
+    const int32_t *block_table;
+    __nv_bfloat16 *out;
+    int32_t *flags;
+    int B, Hq, Hkv, G, q_len, max_pages, num_pages, n_qb;
+    float score_scale;  // sm_scale * log2(e)
+};
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Lane 0 waits (bounded); the verdict is broadcast and every lane then
+// observes the completed phase itself (acquire).  Warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tq,
+                        const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv, const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = bars + 1, *k_empty = k_full + kStages;
+    uint64_t *v_full = k_empty + kStages, *v_empty = v_full + kStages;
+    uint64_t *s_full = v_empty + kStages, *s_free = s_full + 2;
+    uint64_t *p_full = s_free + 2, *o_done = p_full + 1, *mma_done = o_done + 1;
+    uint64_t *xbar = mma_done + 1;
+    float *xch = reinterpret_cast<float *>(smem + kOffX);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // heaviest query blocks (the last ones: the longest causal prefix) first
+    const int per_qb = a.B * a.Hq;
+    const int qb = a.n_qb - 1 - (int)(blockIdx.x / per_qb);
+    const int rem = (int)(blockIdx.x % per_qb);
+    const int r = rem / a.Hq, hq = rem % a.Hq, hkv = hq / a.G;
+    const int i0 = qb * kQB;
+
+    if (threadIdx.x == 0) {
+        // one arrival (an expect-tx arrival or a tcgen05.commit) per phase,
+        // except: every softmax warp frees a score buffer and publishes its
+        // part of P; both warps of a lane quarter join each exchange
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t count = 1;
+            if (&bars[b] == &s_free[0] || &bars[b] == &s_free[1] || &bars[b] == p_full)
+                count = kSoftmaxWarps;
+            else if (&bars[b] >= xbar)
+                count = 2;
+            mbar_init(&bars[b], count);
+        }
+        *abort = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&tq);
+        prefetch_tensormap(&tk);
+        prefetch_tensormap(&tv);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // Q, the caches and the lengths may come from the previous kernel
+
+    int L = __ldg(a.seqlens + r);
+    if (L < 0 || L > a.max_pages * kTile) {
+        if (threadIdx.x == 0 && a.flags && hq == 0 && qb == a.n_qb - 1)
+            atomicOr(a.flags, (int)HPC_FLAG_BAD_SEQLEN);
+        L = min(max(L, 0), a.max_pages * kTile);
+    }
+    const int i_last = min(i0 + kQB - 1, a.q_len - 1);
+    const int lim_max = min(L - a.q_len + i_last, L - 1);  // last visible token of the block
+    const int lim_min = min(L - a.q_len + i0, L - 1);      // ... of its first row
+    const int n = lim_max >= 0 ? lim_max / kKB + 1 : 0;     // KV tiles this CTA reads
+    const int np = (L + kTile - 1) / kTile;                 // pages of the request
+
+    bool ok = true;
+    int q_issued = 0, k_issued[kStages] = {0, 0}, v_issued[kStages] = {0, 0};
+
+    if (warp == kProducerWarp) {
+        const uint64_t pol = policy_evict_normal();
+        if (lane == 0 && n > 0) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)kTileBytes);
+            for (int h = 0; h < 2; ++h)
+                tma_load_4d(smem + kOffQ + h * kHalf, &tq, q_full, 0, h, hq, r * a.q_len + i0,
+                            pol);
+            q_issued = 1;
+        }
+        const int32_t *bt = a.block_table + (size_t)r * a.max_pages;
+        int pg = -1;
+        for (int j = 0; j < n; ++j) {
+            if ((j & 15) == 0) {  // the page numbers of 16 tiles, one per lane
+                const int idx = 2 * j + lane;
+                pg = idx < np ? __ldg(bt + idx) : -1;
+            }
+            const int p0 = __shfl_sync(0xffffffffu, pg, (2 * j) & 31);
+            const int p1 = __shfl_sync(0xffffffffu, pg, (2 * j + 1) & 31);
+            int good = 1;
+            if (lane == 0) {
+                const bool has1 = 2 * j + 1 < np;
+                const bool l0 = p0 >= 0 && p0 < a.num_pages;
+                const bool l1 = has1 && p1 >= 0 && p1 < a.num_pages;
+                if ((!l0 || (has1 && !l1)) && a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_PAGE);
+                const uint32_t bytes = (uint32_t)((l0 ? 1 : 0) + (l1 ? 1 : 0)) * 2 * kTile * 128;
+                const int s = j % kStages;
+                const uint32_t par = ((j / kStages) & 1u) ^ 1u;
+                for (int kv = 0; kv < 2 && good; ++kv) {
+                    uint64_t *full = kv == 0 ? &k_full[s] : &v_full[s];
+                    if (!mbar_wait(kv == 0 ? &k_empty[s] : &v_empty[s], par, abort)) {
+                        good = 0;
+                        break;
+                    }
+                    const CUtensorMap *map = kv == 0 ? &tk : &tv;
+                    uint8_t *dst = smem + (kv == 0 ? kOffK : kOffV) + s * kTileBytes;
+                    if (bytes == 0) {
+                        mbar_arrive(full);
+                    } else {
+                        mbar_arrive_expect_tx(full, bytes);
+                        for (int h = 0; h < 2; ++h) {
+                            if (l0) tma_load_5d(dst + h * kHalf, map, full, 0, h, hkv, 0, p0, pol);
+                            if (l1)
+                                tma_load_5d(dst + h * kHalf + kTile * 128, map, full, 0, h, hkv, 0,
+                                            p1, pol);
+                        }
+                    }
+                    ++(kv == 0 ? k_issued[s] : v_issued[s]);
+                }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                ok = false;
+                break;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        const uint32_t idesc_s = idesc_bf16_f32(kQB, kKB);
+        const uint32_t idesc_o = idesc_bf16_f32_bmn(kQB, kHeadDim);
+        const uint32_t sq = smem_u32(smem + kOffQ), sp = smem_u32(smem + kOffP);
+        if (n > 0 && !warp_wait(q_full, 0, abort)) ok = false;
+        for (int j = 0; ok && j <= n; ++j) {
+            if (j < n) {  // S_j = Q K_j^T into score buffer j mod 2
+                const int s = j % kStages, b = j & 1;
+                if (!warp_wait(&k_full[s], (j / kStages) & 1u, abort) ||
+                    (j >= 2 && !warp_wait(&s_free[b], ((j - 2) >> 1) & 1u, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sk = smem_u32(smem + kOffK + s * kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+                        umma_bf16(tmem + b * kKB, smem_desc_k128(sq + off),
+                                  smem_desc_k128(sk + off), idesc_s, k > 0);
+                    }
+                    umma_commit(&k_empty[s]);
+                    umma_commit(&s_full[b]);
+                }
+                __syncwarp();
+            }
+            if (j >= 1) {  // O += P_t V_t, t = j - 1
+                const int t = j - 1, s = t % kStages;
+                if (!warp_wait(&v_full[s], (t / kStages) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *vs = smem + kOffV + s * kTileBytes;
+                if (t == n - 1 && (t + 1) * kKB > L) {
+                    // tokens past L_r (the last page's free slots, or a page
+                    // the request does not have) must not reach P V: zero
+                    // those rows of both column blocks
+                    const int z0 = L - t * kKB;
+                    for (int h = 0; h < 2; ++h)
+                        for (int e = z0 * 8 + lane; e < kKB * 8; e += 32)
+                            sts128(smem_u32(vs + h * kHalf + e * 16), 0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (!warp_wait(p_full, t & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sv = smem_u32(vs);
+#pragma unroll
+                    for (int k = 0; k < kKB / 16; ++k)
+                        umma_bf16(tmem + kOCol,
+                                  smem_desc_k128(sp + (k >> 2) * kHalf + (k & 3) * 32),
+                                  smem_desc_mn128(sv + k * 16 * 128, kHalf), idesc_o,
+                                  t > 0 || k > 0);
+                    umma_commit(&v_empty[s]);
+                    umma_commit(o_done);
+                }
+                __syncwarp();
+            }
+        }
+        // arrives once every MMA issued has completed (TMEM is freed after it)
+        if (lane == 0) umma_commit(mma_done);
+    } else {
+        // softmax: warp w reads TMEM lanes 32 (w mod 4) .. (its rows) and the
+        // score columns of half w / 4
+        const int q4 = warp & 3, hh = warp >> 2;
+        const int rho = 32 * q4 + lane, i = i0 + rho;
+        const int lim = min(L - a.q_len + i, L - 1);
+        const uint32_t row = tmem + ((uint32_t)(32 * q4) << 16);
+        const float sc = a.score_scale;
+        float m_ref = -INFINITY, l = 0.f;
+        for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            if (!warp_wait(&s_full[b], (j >> 1) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[64];
+            tmem_ld32x2(row + b * kKB + hh * 64, row + b * kKB + hh * 64 + 32, s);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
+            if (j * kKB + kKB - 1 > lim_min) {  // the causal diagonal or the end of the request
+                const int t0 = j * kKB + hh * 64;
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (t0 + c > lim) s[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+            xch[((j & 1) * 2 + hh) * kQB + rho] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[q4]);
+            if (!warp_wait(&xbar[q4], j & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            const float m_tile = fmaxf(mx, xch[((j & 1) * 2 + (hh ^ 1)) * kQB + rho]) * sc;
+            const bool need = m_tile > m_ref + kRescaleLog2;
+            const float new_ref = need ? m_tile : m_ref;
+            const float factor = need ? ex2(m_ref - new_ref) : 1.f;
+            const float base = new_ref == -INFINITY ? 0.f : new_ref;
+            uint32_t pk[32];
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2(fmaf(s[2 * c], sc, -base));
+                const float p1 = ex2(fmaf(s[2 * c + 1], sc, -base));
+                psum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l = l * factor + psum;
+            // P_{j-1} V_{j-1} must be complete before P is overwritten and O rescaled
+            if (j >= 1) {
+                if (!warp_wait(o_done, (j - 1) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
+                    float o[64];
+                    const uint32_t oc = row + kOCol + hh * 64;
+                    tmem_ld32x2(oc, oc + 32, o);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) o[c] *= factor;
+                    tmem_st32x2(oc, oc + 32, o);
+                }
+            }
+            const uint32_t prow = smem_u32(smem + kOffP + hh * kHalf + rho * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                sts128(prow + ((u ^ (rho & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                       pk[4 * u + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            m_ref = new_ref;
+        }
+        // epilogue: O / (sum of both halves' row sums) as BF16
+        float o[64];
+        bool have = ok && n > 0;
+        if (have) {
+            if (!warp_wait(o_done, (n - 1) & 1u, abort)) {
+                ok = have = false;
+            } else {
+                tc_fence_after();
+                xch[((n & 1) * 2 + hh) * kQB + rho] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xbar[q4]);
+                if (!warp_wait(&xbar[q4], n & 1u, abort)) ok = have = false;
+            }
+        }
+        if (have) {
+            const float lt = l + xch[((n & 1) * 2 + (hh ^ 1)) * kQB + rho];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const uint32_t oc = row + kOCol + hh * 64;
+            tmem_ld32x2(oc, oc + 32, o);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) o[c] *= inv;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) o[c] = 0.f;
+        }
+        if (ok && i < a.q_len && !*abort) {
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.out + ((size_t)(r * a.q_len + i) * a.Hq + hq) * kHeadDim + hh * 64);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]),
+                                    pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                                    pack_bf16x2(o[8 * u + 4], o[8 * u + 5]),
+                                    pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+        }
+    }
+
+    if (!ok || *abort) {
+        if (a.flags && lane == 0) atomicOr(a.flags, (int)HPC_FLAG_TIMEOUT);
+        // no copy may land after the CTA has left: wait (bounded) for the last
+        // copy issued into each buffer
+        if (warp == kProducerWarp && lane == 0) {
+            auto drain = [](uint64_t *bar, int issued) {
+                if (issued == 0) return;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar, (uint32_t)(issued - 1) & 1u) &&
+                       globaltimer_ns() - t0 < 1000000000ull) {
+                }
+            };
+            drain(q_full, q_issued);
+            for (int s = 0; s < kStages; ++s) {
+                drain(&k_full[s], k_issued[s]);
+                drain(&v_full[s], v_issued[s]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        // no MMA may still write TMEM when it is freed (bounded, like every wait)
+        if (lane == 0) {
+            volatile int no_abort = 0;
+            mbar_wait(mma_done, 0, &no_abort);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+std::atomic<unsigned> g_prefill_attr_done{0};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over Q [B * q_len, Hq, 128] BF16 as {64 dims, 2 halves, Hq,
+// tokens}, box {64, 1, 1, 128}: one 64-dim half of 128 consecutive query
+// tokens of one head, rows of 128 bytes (the swizzle span).
+hpc_status make_q_map(CUtensorMap *m, const void *q, int64_t tokens, int32_t Hq) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return HPC_ERR_CUDA;
+    std::memset(m, 0, sizeof(*m));
+    cuuint64_t dims[4] = {64, 2, (cuuint64_t)Hq, (cuuint64_t)tokens};
+    cuuint64_t strides[3] = {128, 256, (cuuint64_t)Hq * 256};
+    cuuint32_t box[4] = {64, 1, 1, kQB};
+    cuuint32_t elem[4] = {1, 1, 1, 1};
+    CUresult res = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? HPC_OK : HPC_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace hpc
+
+using namespace hpc;
+
+extern "C" hpc_status hpc_prefill_attn(const void *d_q, const void *d_k_cache,
+                                       const void *d_v_cache, int32_t num_pages,
+                                       const int32_t *d_block_table, int32_t max_pages_per_req,
+                                       const int32_t *d_seqlens, int32_t B, int32_t Hq,
+                                       int32_t Hkv, int32_t head_dim, int32_t q_len,
+                                       float sm_scale, void *d_out, int32_t *d_flags,
+                                       hpc_stream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_req <= 0 || q_len < 1 || num_pages <= 0)
+        return HPC_ERR_ARG;
+    if (head_dim != HPC_HEAD_DIM || Hq % Hkv != 0) return HPC_ERR_UNSUPPORTED;
+    if (!std::isfinite(sm_scale)) return HPC_ERR_ARG;
+    if (B == 0) return HPC_OK;
+    if (!d_q || !d_k_cache || !d_v_cache || !d_block_table || !d_seqlens || !d_out)
+        return HPC_ERR_ARG;
+    if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) || !aligned16(d_out))
+        return HPC_ERR_ARG;
+    const int64_t n_qb = (q_len + kQB - 1) / kQB;
+    const int64_t grid = n_qb * B * Hq;
+    if (grid >= ((int64_t)1 << 31) || (int64_t)B * q_len >= ((int64_t)1 << 31) ||
+        (int64_t)max_pages_per_req * HPC_PAGE_SIZE >= ((int64_t)1 << 30))
+        return HPC_ERR_UNSUPPORTED;
+
+    CUtensorMap tq, tk, tv;
+    hpc_status st = make_q_map(&tq, d_q, (int64_t)B * q_len, Hq);
+    if (st == HPC_OK) st = cache_tensor_map(&tk, d_k_cache, num_pages, Hkv, false);
+    if (st == HPC_OK) st = cache_tensor_map(&tv, d_v_cache, num_pages, Hkv, false);
+    if (st != HPC_OK) return st;
+
+    PrefillArgs a;
+    a.seqlens = d_seqlens;
+    a.block_table = d_block_table;
+    a.out = static_cast<__nv_bfloat16 *>(d_out);
+    a.flags = d_flags;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.q_len = q_len;
+    a.max_pages = max_pages_per_req;
+    a.num_pages = num_pages;
+    a.n_qb = (int)n_qb;
+    a.score_scale = sm_scale * 1.4426950408889634f;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
+    const unsigned bit = 1u << (dev & 31);
+    if (!(g_prefill_attr_done.load() & bit)) {
+        if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return HPC_ERR_CUDA;
+        g_prefill_attr_done.fetch_or(bit);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_attn_kernel, tq, tk, tv, a);
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}

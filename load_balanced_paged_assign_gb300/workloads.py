@@ -102,6 +102,27 @@ for _i, (_name, _draw) in enumerate(TABLE3.items()):
                                 description=f"Table-3 mix {_name[3:]}, FP8, Hq=8, Hkv=1")
 
 
+# The prefill and extend rows of the vLLM post's attention comparison (Table
+# 4): "qAsB" is q_len = A new tokens over a request of B tokens (a cached
+# prefix of B - A), "qA prefill" is q_len = L = A, the leading number is the
+# batch.  The table gives neither heads nor precision; these take Hy3's TP1
+# GQA shape (64 query heads, 8 KV heads, head dim 128) in BF16.
+TABLE4_PREFILL = {
+    "t4_q512": (1, 512, 512),
+    "t4_q1ks2k": (1, 1024, 2048),
+    "t4_q2k": (1, 2048, 2048),
+    "t4_q4k": (1, 4096, 4096),
+    "t4_q8k": (1, 8192, 8192),
+    "t4_2q1ks4k": (2, 1024, 4096),
+}
+for _i, (_name, (_b, _q, _l)) in enumerate(TABLE4_PREFILL.items()):
+    WORKLOADS[_name] = Workload(_name, _b, 64, 8, draw=((_b, "fixed", _l, _l),), seed=1300 + _i,
+                                q_len=_q,
+                                description=f"Table-4 {'extend' if _q < _l else 'prefill'} "
+                                            f"{_name[3:]}: B={_b}, q_len={_q}, L={_l}, Hq=64, "
+                                            f"Hkv=8, BF16")
+
+
 def draw_seqlens(w: Workload, gen: torch.Generator) -> list:
     if w.seqlens:
         return [int(x) for x in w.seqlens]
