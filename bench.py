@@ -10,8 +10,12 @@ to its CUDA-event duration and the measured HBM copy peak; `e2e` is the same
 step through the host-buffer C entry point with the per-step inputs copied in
 and the output copied out inside the timed region; `cpu_baseline` is the fp64
 oracle timed on a bounded sample on the host cores; `static` is the in-house
-static split-KV schedule on the same batch.  Under torchrun every rank runs
-an independent replica (the path has no exchange step).
+static split-KV schedule on the same batch.  Side legs: the fused prologue
+(`rope_norm`), multi-query decode (`mtp`), the router GEMM sweep
+(`router_gemm`) and extend / prefill attention on the vLLM comparison's
+shapes (`prefill`, TFLOP/s against the measured BF16 tensor peak).  Under
+torchrun every rank runs an independent replica (the path has no exchange
+step).
 """
 
 from __future__ import annotations
@@ -110,6 +114,21 @@ def router_cost(M, N, K, splits):
     flops = 2 * 2 * M * N * K
     nbytes = M * K * 2 + 2 * N * K * 2 + M * N * 4 + (2 * splits * M * N * 4 if splits > 1 else 0)
     return flops, nbytes
+
+
+def prefill_flops(seqlens, q_len, Hq):
+    """FLOPs of causal extend / prefill attention: query token i of a request
+    of L tokens sees max(0, L - q_len + 1 + i) tokens; each (row, token) pair
+    costs 2 * 128 for Q K^T and 2 * 128 for P V."""
+    pairs = 0
+    for L in seqlens:
+        for_all = max(0, L - q_len + 1)  # tokens seen by query 0 (when L >= q_len)
+        if L >= q_len:
+            pairs += q_len * for_all + q_len * (q_len - 1) // 2
+        else:
+            n = L  # queries q_len - L .. q_len - 1 see 1 .. L tokens
+            pairs += n * (n + 1) // 2
+    return 4 * 128 * Hq * pairs
 
 
 def profiled_traffic(kernel_src_hash, kv_dtype, workload):
@@ -256,6 +275,9 @@ def parse_args():
     ap.add_argument("--no-prologue", action="store_true")
     ap.add_argument("--no-mtp", action="store_true")
     ap.add_argument("--no-router", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-shapes", default="",
+                    help="comma-separated prefill/extend workloads (default: all of Table 4's)")
     ap.add_argument("--floor", type=int, default=None)
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
@@ -665,6 +687,61 @@ def main():
                                                           "hbm_gbs": peak, "kind": tf_kind},
                   "sweep": rows}
 
+    # ---- extend / prefill attention (tcgen05) on the vLLM comparison's
+    # prefill and extend shapes.  torch's scaled_dot_product_attention on
+    # contiguous copies (K/V expanded to the query heads) is timed beside the
+    # prefills as context: a library kernel on the same GPU, not the path.
+    prefill = None
+    if not args.no_prefill:
+        from load_balanced_paged_assign_gb300.workloads import TABLE4_PREFILL
+        tf_peak, tf_kind = measured_bf16_tflops()
+        rows = []
+        n_p = min(args.steps, 50)
+        shapes = [x for x in args.prefill_shapes.split(",") if x] or list(TABLE4_PREFILL)
+        for name in shapes:
+            wp = WORKLOADS[name]
+            bp = make_batch(wp, device=dev)
+            Bp, qn, Hqp, Hkvp = int(bp.seqlens.numel()), wp.q_len, wp.num_q_heads, wp.num_kv_heads
+            lens_p = bp.seqlens.cpu().tolist()
+            outp = torch.empty((Bp, qn, Hqp, 128), dtype=torch.bfloat16, device=dev)
+            pflags = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def prefill_call():
+                hd.hpc_prefill_attn(bp.q, bp.k_cache, bp.v_cache, bp.block_table, bp.seqlens,
+                                    Hqp, Hkvp, qn, wp.sm_scale, outp, flags=pflags)
+
+            us = statistics.fmean(timed(n_p, args.warmup, prefill_call))
+            if int(pflags.item()) != 0:
+                raise RuntimeError(f"prefill error flags {int(pflags.item())}")
+            flops = prefill_flops(lens_p, qn, Hqp)
+            tfl = flops / (us * 1e-6) / 1e12
+            row = {"workload": name, "batch": Bp, "q_len": qn, "seqlen": lens_p[0],
+                   "us": us, "flops": flops, "tflops": tfl, "frac": tfl / tf_peak}
+            if all(L == qn for L in lens_p) and Bp == 1:
+                try:
+                    npg = (qn + 63) // 64
+                    pages = bp.block_table[0, :npg].long()
+                    kc = bp.k_cache[pages].reshape(npg * 64, Hkvp, 128)[:qn]
+                    vc = bp.v_cache[pages].reshape(npg * 64, Hkvp, 128)[:qn]
+                    G = Hqp // Hkvp
+                    qs = bp.q[0].transpose(0, 1).contiguous()[None]
+                    ks = kc.repeat_interleave(G, dim=1).transpose(0, 1).contiguous()[None]
+                    vs = vc.repeat_interleave(G, dim=1).transpose(0, 1).contiguous()[None]
+                    sdpa = torch.nn.functional.scaled_dot_product_attention
+                    t_us = statistics.fmean(timed(n_p, args.warmup, lambda: sdpa(
+                        qs, ks, vs, is_causal=True, scale=wp.sm_scale)))
+                    row["torch_sdpa_us"] = t_us
+                    row["speedup_vs_torch_sdpa"] = t_us / us
+                    del qs, ks, vs, kc, vc
+                except RuntimeError as exc:  # no fused kernel for this shape: leave it out
+                    row["torch_sdpa_us"] = None
+                    row["torch_sdpa_error"] = str(exc)[:120]
+            rows.append(row)
+            del bp, outp
+        prefill = {"heads": "Hq=64, Hkv=8, head_dim 128, BF16 (Hy3 TP1 shape)",
+                   "peak_bf16_tflops": tf_peak, "peak_kind": tf_kind,
+                   "l2": "flushed before every call", "shapes": rows}
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
@@ -699,6 +776,7 @@ def main():
         "rope_norm": prologue,
         "mtp": mtp,
         "router_gemm": router,
+        "prefill": prefill,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }
