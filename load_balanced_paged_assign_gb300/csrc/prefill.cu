@@ -8,25 +8,30 @@
 // prefix before the new tokens.
 //
 // GB300 design (tcgen05 + TMEM + TMA), one CTA per (request, query head,
-// block of 128 query tokens), heaviest (last) query blocks first:
-//   * warp 8 loads the CTA's Q tile once and then streams 128-token K and V
-//     tiles (two 64-token pages each, gathered through the block table) into
-//     two-stage rings with TMA (128-byte swizzle);
-//   * one thread of warp 9 issues tcgen05.mma: S_j = Q K_j^T into one of two
-//     TMEM score buffers, then O += P_{j-1} V_{j-1} into the TMEM output
-//     accumulator (V read as an MN-major operand straight from its cache
-//     layout), so the tensor cores compute the next scores while the softmax
-//     warps work on the current ones;
-//   * warps 0-7 run the online softmax, two warps per TMEM lane quarter (a
-//     row's 128 scores split into two halves of 64, their maxima exchanged
-//     through shared memory): they read S with tcgen05.ld, mask the causal
-//     diagonal, and write P = exp2(S * scale * log2 e - m) as BF16 into the
-//     shared-memory operand of the next PV product.  The running maximum m
-//     moves only when a tile's maximum exceeds it by more than 8 (log2
-//     units), so P stays <= 256 and the accumulator is rescaled (tcgen05.ld,
-//     multiply, tcgen05.st) only on those rare tiles; the result is the same
-//     softmax, since O and the row sum always share the reference m;
+// pair of 128-token query tiles), heaviest (last) pairs first:
+//   * warp 8 loads the CTA's two Q tiles once and then streams 128-token K
+//     and V tiles (two 64-token pages each, gathered through the block table)
+//     into two-stage rings with TMA (128-byte swizzle);
+//   * one thread of warp 9 issues tcgen05.mma.  Per KV tile j and Q tile x:
+//     S_x = Q_x K_j^T (both operands in shared memory) into x's TMEM score
+//     columns, and once the softmax has turned them into P_x, O_x += P_x V_j
+//     with P_x read straight from TMEM and V from its cache layout (an
+//     MN-major shared-memory operand).  The two Q tiles share every K/V tile
+//     and alternate on the tensor cores: x's next scores are issued right
+//     behind x's PV product, while the other tile's softmax runs;
+//   * warps 0-3 run the online softmax of Q tile 0 and warps 4-7 that of Q
+//     tile 1, one thread per query row (warp w reads TMEM lanes 32 (w mod 4)
+//     ..): tcgen05.ld of the row's 128 scores, the causal mask on the
+//     diagonal, P = exp2(S * scale * log2 e - m) packed to BF16 and written
+//     over the scores with tcgen05.st.  The running maximum m moves only when
+//     a tile's maximum exceeds it by more than 8 (log2 units), so P stays <=
+//     256 and the accumulator is rescaled (tcgen05.ld, multiply, tcgen05.st)
+//     only on those rare tiles; the result is the same softmax, since O and
+//     the row sum always share the reference m;
 //   * the epilogue divides O by the row sum and writes BF16.
+// A tcgen05.commit covers every MMA its thread issued before it, so when x's
+// scores for tile j are complete, x's product with tile j - 1 is complete
+// too: the softmax may read and rescale O_x without a further wait.
 // Every mbarrier wait is bounded; on a timeout the CTA raises the error flag,
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and leaves.
 #include <cuda_bf16.h>
@@ -42,37 +47,36 @@
 namespace hpc {
 namespace {
 
-constexpr int kQB = 128;                   // query rows per CTA (UMMA M)
-constexpr int kKB = 128;                   // KV tokens per tile
-constexpr int kHalf = 128 * 128;           // bytes of 128 rows x 64 BF16 (one 128-byte column block)
-constexpr int kTileBytes = 2 * kHalf;      // a 128 x 128 BF16 tile
-constexpr int kStages = 2;                 // K ring and V ring depth
-constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kQB = 128;                 // query rows per Q tile (UMMA M)
+constexpr int kQT = 2;                   // Q tiles per CTA
+constexpr int kKB = 128;                 // KV tokens per tile: two pages
+constexpr int kHalf = 128 * 128;         // 128 rows x 64 BF16: one 128-byte column block
+constexpr int kTileBytes = 2 * kHalf;    // a 128 x 128 BF16 tile (Q, K or V)
+constexpr int kStages = 2;               // K ring and V ring depth
+constexpr int kSoftmaxWarps = 4 * kQT;
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr uint32_t kTmemCols = 512;        // S0 [0, 128), S1 [128, 256), O [256, 384)
+constexpr uint32_t kTmemCols = 512;      // S_x / P_x at 128 x; O_x at 256 + 128 x
 constexpr int kOCol = 256;
-constexpr float kRescaleLog2 = 8.f;        // P <= 2^8 between reference moves
+constexpr float kRescaleLog2 = 8.f;      // P <= 2^8 between reference moves
 
 // Shared-memory layout (offsets from the 1024-byte aligned base).
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffK = kOffQ + kQT * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-// s_free[2], p_full, o_done, mma_done, xbar[4]
-constexpr int kNumBars = 1 + 2 * kStages * 2 + 2 + 2 + 3 + 4;
-constexpr int kOffX = kOffBar + kNumBars * 8;              // float [2][2][128] exchange
-constexpr int kOffMisc = kOffX + 2 * 2 * kQB * 4;          // tmem slot, abort word
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;           // + alignment slack
+// p_full[2], o_done[2], mma_done
+constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort word
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
 struct PrefillArgs {
     const int32_t *seqlens;
     const int32_t *block_table;
     __nv_bfloat16 *out;
     int32_t *flags;
-    int B, Hq, Hkv, G, q_len, max_pages, num_pages, n_qb;
+    int B, Hq, Hkv, G, q_len, max_pages, num_pages, n_qp;
     float score_scale;  // sm_scale * log2(e)
 };
 
@@ -99,6 +103,24 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
+// The causal extent of a Q tile: its first query row, the KV tiles its rows
+// read, and the last token its first row sees.
+struct QTile {
+    int first, tiles, lim_first;
+};
+
+__device__ __forceinline__ QTile qtile(int i0, int L, int q_len) {
+    QTile t;
+    t.first = i0;
+    t.lim_first = min(L - q_len + i0, L - 1);
+    t.tiles = 0;
+    if (i0 < q_len) {
+        const int lim_last = min(L - q_len + min(i0 + kQB - 1, q_len - 1), L - 1);
+        t.tiles = lim_last >= 0 ? lim_last / kKB + 1 : 0;
+    }
+    return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tq,
                         const __grid_constant__ CUtensorMap tk,
@@ -110,32 +132,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars;
     uint64_t *k_full = bars + 1, *k_empty = k_full + kStages;
     uint64_t *v_full = k_empty + kStages, *v_empty = v_full + kStages;
-    uint64_t *s_full = v_empty + kStages, *s_free = s_full + 2;
-    uint64_t *p_full = s_free + 2, *o_done = p_full + 1, *mma_done = o_done + 1;
-    uint64_t *xbar = mma_done + 1;
-    float *xch = reinterpret_cast<float *>(smem + kOffX);
+    uint64_t *s_full = v_empty + kStages;  // [x]: S_x complete (and every MMA before it)
+    uint64_t *p_full = s_full + kQT;       // [x]: P_x written (four warps)
+    uint64_t *o_done = p_full + kQT;       // [x]: O_x += P_x V complete
+    uint64_t *mma_done = o_done + kQT;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // heaviest query blocks (the last ones: the longest causal prefix) first
-    const int per_qb = a.B * a.Hq;
-    const int qb = a.n_qb - 1 - (int)(blockIdx.x / per_qb);
-    const int rem = (int)(blockIdx.x % per_qb);
+    // heaviest query tiles (the last ones: the longest causal prefix) first
+    const int per_qp = a.B * a.Hq;
+    const int qp = a.n_qp - 1 - (int)(blockIdx.x / per_qp);
+    const int rem = (int)(blockIdx.x % per_qp);
     const int r = rem / a.Hq, hq = rem % a.Hq, hkv = hq / a.G;
-    const int i0 = qb * kQB;
+    const int i0 = qp * kQT * kQB;
 
     if (threadIdx.x == 0) {
         // one arrival (an expect-tx arrival or a tcgen05.commit) per phase,
-        // except: every softmax warp frees a score buffer and publishes its
-        // part of P; both warps of a lane quarter join each exchange
+        // except that all four warps of a Q tile publish its P
         for (int b = 0; b < kNumBars; ++b) {
-            uint32_t count = 1;
-            if (&bars[b] == &s_free[0] || &bars[b] == &s_free[1] || &bars[b] == p_full)
-                count = kSoftmaxWarps;
-            else if (&bars[b] >= xbar)
-                count = 2;
-            mbar_init(&bars[b], count);
+            const bool per_warp = &bars[b] >= p_full && &bars[b] < o_done;
+            mbar_init(&bars[b], per_warp ? 4 : 1);
         }
         *abort = 0;
         fence_barrier_init();
@@ -155,26 +172,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int L = __ldg(a.seqlens + r);
     if (L < 0 || L > a.max_pages * kTile) {
-        if (threadIdx.x == 0 && a.flags && hq == 0 && qb == a.n_qb - 1)
+        if (threadIdx.x == 0 && a.flags && hq == 0 && qp == a.n_qp - 1)
             atomicOr(a.flags, (int)HPC_FLAG_BAD_SEQLEN);
         L = min(max(L, 0), a.max_pages * kTile);
     }
-    const int i_last = min(i0 + kQB - 1, a.q_len - 1);
-    const int lim_max = min(L - a.q_len + i_last, L - 1);  // last visible token of the block
-    const int lim_min = min(L - a.q_len + i0, L - 1);      // ... of its first row
-    const int n = lim_max >= 0 ? lim_max / kKB + 1 : 0;     // KV tiles this CTA reads
-    const int np = (L + kTile - 1) / kTile;                 // pages of the request
+    QTile qt[kQT];
+#pragma unroll
+    for (int x = 0; x < kQT; ++x) qt[x] = qtile(i0 + x * kQB, L, a.q_len);
+    int n = 0;  // KV tiles the CTA reads
+#pragma unroll
+    for (int x = 0; x < kQT; ++x) n = max(n, qt[x].tiles);
+    const int np = (L + kTile - 1) / kTile;  // pages of the request
 
     bool ok = true;
-    int q_issued = 0, k_issued[kStages] = {0, 0}, v_issued[kStages] = {0, 0};
+    int q_issued = 0, k_issued[kStages] = {}, v_issued[kStages] = {};
 
     if (warp == kProducerWarp) {
         const uint64_t pol = policy_evict_normal();
         if (lane == 0 && n > 0) {
-            mbar_arrive_expect_tx(q_full, (uint32_t)kTileBytes);
-            for (int h = 0; h < 2; ++h)
-                tma_load_4d(smem + kOffQ + h * kHalf, &tq, q_full, 0, h, hq, r * a.q_len + i0,
-                            pol);
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int x = 0; x < kQT; ++x) bytes += qt[x].tiles > 0 ? kTileBytes : 0;
+            mbar_arrive_expect_tx(q_full, bytes);
+#pragma unroll
+            for (int x = 0; x < kQT; ++x)
+                if (qt[x].tiles > 0)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(smem + kOffQ + x * kTileBytes + h * kHalf, &tq, q_full, 0, h,
+                                    hq, r * a.q_len + qt[x].first, pol);
             q_issued = 1;
         }
         const int32_t *bt = a.block_table + (size_t)r * a.max_pages;
@@ -201,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         good = 0;
                         break;
                     }
-                    const CUtensorMap *map = kv == 0 ? &tk : &tv;
-                    uint8_t *dst = smem + (kv == 0 ? kOffK : kOffV) + s * kTileBytes;
                     if (bytes == 0) {
                         mbar_arrive(full);
                     } else {
                         mbar_arrive_expect_tx(full, bytes);
+                        const CUtensorMap *map = kv == 0 ? &tk : &tv;
+                        uint8_t *dst = smem + (kv == 0 ? kOffK : kOffV) + s * kTileBytes;
                         for (int h = 0; h < 2; ++h) {
                             if (l0) tma_load_5d(dst + h * kHalf, map, full, 0, h, hkv, 0, p0, pol);
                             if (l1)
@@ -226,182 +251,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         const uint32_t idesc_s = idesc_bf16_f32(kQB, kKB);
         const uint32_t idesc_o = idesc_bf16_f32_bmn(kQB, kHeadDim);
-        const uint32_t sq = smem_u32(smem + kOffQ), sp = smem_u32(smem + kOffP);
-        if (n > 0 && !warp_wait(q_full, 0, abort)) ok = false;
-        for (int j = 0; ok && j <= n; ++j) {
-            if (j < n) {  // S_j = Q K_j^T into score buffer j mod 2
-                const int s = j % kStages, b = j & 1;
-                if (!warp_wait(&k_full[s], (j / kStages) & 1u, abort) ||
-                    (j >= 2 && !warp_wait(&s_free[b], ((j - 2) >> 1) & 1u, abort))) {
+        // descriptor bases: the K-step offsets below are compile-time
+        // additions to the start-address field (addresses stay < 256 KB)
+        const uint64_t dq0 = smem_desc_k128(smem_u32(smem + kOffQ));
+        const uint64_t dk0 = smem_desc_k128(smem_u32(smem + kOffK));
+        const uint64_t dv0 = smem_desc_mn128(smem_u32(smem + kOffV), kHalf);
+        // S_x = Q_x K^T into x's score columns (K tile in stage s)
+        auto issue_s = [&](int x, int s) {
+            const uint64_t dq = dq0 + (uint64_t)((x * kTileBytes) >> 4);
+            const uint64_t dk = dk0 + (uint64_t)((s * kTileBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+                const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
+                umma_bf16(tmem + 128 * x, dq + off, dk + off, idesc_s, k > 0);
+            }
+            umma_commit(&s_full[x]);
+        };
+        // O_x += P_x V (V tile in stage s), P_x from TMEM
+        auto issue_pv = [&](int x, int s, bool acc) {
+            const uint64_t dv = dv0 + (uint64_t)((s * kTileBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < kKB / 16; ++k)
+                umma_bf16_ts(tmem + kOCol + 128 * x, tmem + 128 * x + 8 * k,
+                             dv + (uint64_t)((k * 16 * 128) >> 4), idesc_o, acc || k > 0);
+            umma_commit(&o_done[x]);
+        };
+        if (n > 0) {
+            if (!warp_wait(q_full, 0, abort) || !warp_wait(&k_full[0], 0, abort)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                if (lane == 0) {
+                    for (int x = 0; x < kQT; ++x)
+                        if (qt[x].tiles > 0) issue_s(x, 0);
+                    umma_commit(&k_empty[0]);
+                }
+                __syncwarp();
+            }
+        }
+        for (int j = 0; ok && j < n; ++j) {
+            const int s = j % kStages, s1 = (j + 1) % kStages;
+            if (!warp_wait(&v_full[s], (j / kStages) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            uint8_t *vs = smem + kOffV + s * kTileBytes;
+            if (j == n - 1 && (j + 1) * kKB > L) {
+                // tokens past L_r (the last page's free slots, or a page the
+                // request does not have) must not reach P V: zero those rows
+                // of both column blocks
+                const int z0 = L - j * kKB;
+                for (int h = 0; h < 2; ++h)
+                    for (int e = z0 * 8 + lane; e < kKB * 8; e += 32)
+                        sts128(smem_u32(vs + h * kHalf + e * 16), 0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            const bool next = j + 1 < n;
+            if (next && !warp_wait(&k_full[s1], ((j + 1) / kStages) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            for (int x = 0; x < kQT && ok; ++x) {
+                if (j >= qt[x].tiles) continue;
+                if (!warp_wait(&p_full[x], j & 1u, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sk = smem_u32(smem + kOffK + s * kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-                        umma_bf16(tmem + b * kKB, smem_desc_k128(sq + off),
-                                  smem_desc_k128(sk + off), idesc_s, k > 0);
-                    }
-                    umma_commit(&k_empty[s]);
-                    umma_commit(&s_full[b]);
+                    issue_pv(x, s, j > 0);
+                    if (j + 1 < qt[x].tiles) issue_s(x, s1);
                 }
                 __syncwarp();
             }
-            if (j >= 1) {  // O += P_t V_t, t = j - 1
-                const int t = j - 1, s = t % kStages;
-                if (!warp_wait(&v_full[s], (t / kStages) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *vs = smem + kOffV + s * kTileBytes;
-                if (t == n - 1 && (t + 1) * kKB > L) {
-                    // tokens past L_r (the last page's free slots, or a page
-                    // the request does not have) must not reach P V: zero
-                    // those rows of both column blocks
-                    const int z0 = L - t * kKB;
-                    for (int h = 0; h < 2; ++h)
-                        for (int e = z0 * 8 + lane; e < kKB * 8; e += 32)
-                            sts128(smem_u32(vs + h * kHalf + e * 16), 0u, 0u, 0u, 0u);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (!warp_wait(p_full, t & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sv = smem_u32(vs);
-#pragma unroll
-                    for (int k = 0; k < kKB / 16; ++k)
-                        umma_bf16(tmem + kOCol,
-                                  smem_desc_k128(sp + (k >> 2) * kHalf + (k & 3) * 32),
-                                  smem_desc_mn128(sv + k * 16 * 128, kHalf), idesc_o,
-                                  t > 0 || k > 0);
-                    umma_commit(&v_empty[s]);
-                    umma_commit(o_done);
-                }
-                __syncwarp();
+            if (!ok) break;
+            if (lane == 0) {
+                umma_commit(&v_empty[s]);  // after both Q tiles' products with V_j
+                if (next) umma_commit(&k_empty[s1]);  // after both Q tiles' scores with K_j+1
             }
+            __syncwarp();
         }
         // arrives once every MMA issued has completed (TMEM is freed after it)
         if (lane == 0) umma_commit(mma_done);
     } else {
-        // softmax: warp w reads TMEM lanes 32 (w mod 4) .. (its rows) and the
-        // score columns of half w / 4
-        const int q4 = warp & 3, hh = warp >> 2;
-        const int rho = 32 * q4 + lane, i = i0 + rho;
+        // softmax of Q tile x: thread = one query row, warp w reads TMEM
+        // lanes 32 (w mod 4) ..
+        const int x = warp >> 2, q4 = warp & 3;
+        const QTile t = qt[x];
+        const int rho = 32 * q4 + lane, i = t.first + rho;
         const int lim = min(L - a.q_len + i, L - 1);
         const uint32_t row = tmem + ((uint32_t)(32 * q4) << 16);
+        const uint32_t scol = row + 128 * x, ocol = row + kOCol + 128 * x;
         const float sc = a.score_scale;
         float m_ref = -INFINITY, l = 0.f;
-        for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
-            if (!warp_wait(&s_full[b], (j >> 1) & 1u, abort)) {
+        for (int j = 0; j < t.tiles; ++j) {
+            if (!warp_wait(&s_full[x], j & 1u, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[64];
-            tmem_ld32x2(row + b * kKB + hh * 64, row + b * kKB + hh * 64 + 32, s);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
-            if (j * kKB + kKB - 1 > lim_min) {  // the causal diagonal or the end of the request
-                const int t0 = j * kKB + hh * 64;
+            float s[128];
+            tmem_ld32x2(scol, scol + 32, *reinterpret_cast<float(*)[64]>(s));
+            tmem_ld32x2(scol + 64, scol + 96, *reinterpret_cast<float(*)[64]>(s + 64));
+            if (j * kKB + kKB - 1 > t.lim_first) {  // the causal diagonal or the request's end
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (t0 + c > lim) s[c] = -INFINITY;
+                for (int c = 0; c < 128; ++c)
+                    if (j * kKB + c > lim) s[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
-            xch[((j & 1) * 2 + hh) * kQB + rho] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar[q4]);
-            if (!warp_wait(&xbar[q4], j & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            const float m_tile = fmaxf(mx, xch[((j & 1) * 2 + (hh ^ 1)) * kQB + rho]) * sc;
+            for (int c = 0; c < 128; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float m_tile = mx * sc;
             const bool need = m_tile > m_ref + kRescaleLog2;
             const float new_ref = need ? m_tile : m_ref;
             const float factor = need ? ex2(m_ref - new_ref) : 1.f;
             const float base = new_ref == -INFINITY ? 0.f : new_ref;
-            uint32_t pk[32];
-            float psum = 0.f;
+            float pk[64];  // P as packed BF16 pairs (bit patterns)
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 64; ++c) {
                 const float p0 = ex2(fmaf(s[2 * c], sc, -base));
                 const float p1 = ex2(fmaf(s[2 * c + 1], sc, -base));
-                psum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+                ps[c & 3] += p0 + p1;
+                pk[c] = __uint_as_float(pack_bf16x2(p0, p1));
             }
-            l = l * factor + psum;
-            // P_{j-1} V_{j-1} must be complete before P is overwritten and O rescaled
-            if (j >= 1) {
-                if (!warp_wait(o_done, (j - 1) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
+            l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+            // O_x is settled: its product with the previous tile completed
+            // before these scores did
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
                     float o[64];
-                    const uint32_t oc = row + kOCol + hh * 64;
-                    tmem_ld32x2(oc, oc + 32, o);
+                    tmem_ld32x2(ocol + 64 * hf, ocol + 64 * hf + 32, o);
 #pragma unroll
                     for (int c = 0; c < 64; ++c) o[c] *= factor;
-                    tmem_st32x2(oc, oc + 32, o);
+                    tmem_st32x2(ocol + 64 * hf, ocol + 64 * hf + 32, o);
                 }
             }
-            const uint32_t prow = smem_u32(smem + kOffP + hh * kHalf + rho * 128);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                sts128(prow + ((u ^ (rho & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                       pk[4 * u + 3]);
-            fence_proxy_async_smem();
+            tmem_st32x2(scol, scol + 32, pk);  // P over the first 64 score columns
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[x]);
             m_ref = new_ref;
         }
-        // epilogue: O / (sum of both halves' row sums) as BF16
-        float o[64];
-        bool have = ok && n > 0;
+        // epilogue: O / l as BF16
+        bool have = ok && t.tiles > 0;
         if (have) {
-            if (!warp_wait(o_done, (n - 1) & 1u, abort)) {
+            if (!warp_wait(&o_done[x], (t.tiles - 1) & 1u, abort))
                 ok = have = false;
-            } else {
+            else
                 tc_fence_after();
-                xch[((n & 1) * 2 + hh) * kQB + rho] = l;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xbar[q4]);
-                if (!warp_wait(&xbar[q4], n & 1u, abort)) ok = have = false;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool store = ok && i < a.q_len;
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            a.out + ((size_t)(r * a.q_len + min(i, a.q_len - 1)) * a.Hq + hq) * kHeadDim);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float o[64];
+            if (have) {
+                tmem_ld32x2(ocol + 64 * hf, ocol + 64 * hf + 32, o);
+#pragma unroll
+                for (int c = 0; c < 64; ++c) o[c] *= inv;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) o[c] = 0.f;
             }
-        }
-        if (have) {
-            const float lt = l + xch[((n & 1) * 2 + (hh ^ 1)) * kQB + rho];
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const uint32_t oc = row + kOCol + hh * 64;
-            tmem_ld32x2(oc, oc + 32, o);
+            if (store && !*abort) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) o[c] *= inv;
-        } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) o[c] = 0.f;
-        }
-        if (ok && i < a.q_len && !*abort) {
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.out + ((size_t)(r * a.q_len + i) * a.Hq + hq) * kHeadDim + hh * 64);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                dst[u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]),
-                                    pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
-                                    pack_bf16x2(o[8 * u + 4], o[8 * u + 5]),
-                                    pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+                for (int u = 0; u < 8; ++u)
+                    dst[8 * hf + u] = make_uint4(pack_bf16x2(o[8 * u], o[8 * u + 1]),
+                                                 pack_bf16x2(o[8 * u + 2], o[8 * u + 3]),
+                                                 pack_bf16x2(o[8 * u + 4], o[8 * u + 5]),
+                                                 pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+            }
         }
     }
 
@@ -481,8 +505,8 @@ extern "C" hpc_status hpc_prefill_attn(const void *d_q, const void *d_k_cache,
         return HPC_ERR_ARG;
     if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) || !aligned16(d_out))
         return HPC_ERR_ARG;
-    const int64_t n_qb = (q_len + kQB - 1) / kQB;
-    const int64_t grid = n_qb * B * Hq;
+    const int64_t n_qp = (q_len + kQT * kQB - 1) / (kQT * kQB);
+    const int64_t grid = n_qp * B * Hq;
     if (grid >= ((int64_t)1 << 31) || (int64_t)B * q_len >= ((int64_t)1 << 31) ||
         (int64_t)max_pages_per_req * HPC_PAGE_SIZE >= ((int64_t)1 << 30))
         return HPC_ERR_UNSUPPORTED;
@@ -505,7 +529,7 @@ extern "C" hpc_status hpc_prefill_attn(const void *d_q, const void *d_k_cache,
     a.q_len = q_len;
     a.max_pages = max_pages_per_req;
     a.num_pages = num_pages;
-    a.n_qb = (int)n_qb;
+    a.n_qp = (int)n_qp;
     a.score_scale = sm_scale * 1.4426950408889634f;
 
     int dev = 0;
