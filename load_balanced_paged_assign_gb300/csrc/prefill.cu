@@ -66,8 +66,8 @@ constexpr int kOffK = kOffQ + kQT * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-// p_full[2], o_done[2], mma_done
-constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 1;
+// p_full[2], o_done[2], mma_done, v_tail
+constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort word
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + kQT;       // [x]: P_x written (four warps)
     uint64_t *o_done = p_full + kQT;       // [x]: O_x += P_x V complete
     uint64_t *mma_done = o_done + kQT;
+    uint64_t *v_tail = mma_done + 1;       // the last V tile with its free slots zeroed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int x = 0; x < kQT; ++x) n = max(n, qt[x].tiles);
     const int np = (L + kTile - 1) / kTile;  // pages of the request
+    const bool tail = n > 0 && n * kKB > L;   // the last tile holds slots past L_r
 
     bool ok = true;
     int q_issued = 0, k_issued[kStages] = {}, v_issued[kStages] = {};
@@ -248,6 +250,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
         }
+        if (ok && tail) {
+            // tokens past L_r (the last page's free slots, or a page the
+            // request does not have) must not reach P V: once the last V
+            // tile has landed, zero those rows of both column blocks
+            const int jl = n - 1, s = jl % kStages;
+            if (!warp_wait(&v_full[s], (jl / kStages) & 1u, abort)) {
+                ok = false;
+            } else {
+                uint8_t *vs = smem + kOffV + s * kTileBytes;
+                const int z0 = L - jl * kKB;
+                for (int h = 0; h < 2; ++h)
+                    for (int e = z0 * 8 + lane; e < kKB * 8; e += 32)
+                        sts128(smem_u32(vs + h * kHalf + e * 16), 0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_tail);
+            }
+        }
     } else if (warp == kMmaWarp) {
         const uint32_t idesc_s = idesc_bf16_f32(kQB, kKB);
         const uint32_t idesc_o = idesc_bf16_f32_bmn(kQB, kHeadDim);
@@ -276,61 +296,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                              dv + (uint64_t)((k * 16 * 128) >> 4), idesc_o, acc || k > 0);
             umma_commit(&o_done[x]);
         };
-        if (n > 0) {
-            if (!warp_wait(q_full, 0, abort) || !warp_wait(&k_full[0], 0, abort)) ok = false;
-            if (ok) {
-                tc_fence_after();
-                if (lane == 0) {
+        // one thread issues everything; every wait is its own (bounded)
+        if (lane == 0) {
+            if (n > 0) {
+                ok = mbar_wait(q_full, 0, abort) && mbar_wait(&k_full[0], 0, abort);
+                if (ok) {
+                    tc_fence_after();
                     for (int x = 0; x < kQT; ++x)
                         if (qt[x].tiles > 0) issue_s(x, 0);
                     umma_commit(&k_empty[0]);
                 }
-                __syncwarp();
             }
-        }
-        for (int j = 0; ok && j < n; ++j) {
-            const int s = j % kStages, s1 = (j + 1) % kStages;
-            if (!warp_wait(&v_full[s], (j / kStages) & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            uint8_t *vs = smem + kOffV + s * kTileBytes;
-            if (j == n - 1 && (j + 1) * kKB > L) {
-                // tokens past L_r (the last page's free slots, or a page the
-                // request does not have) must not reach P V: zero those rows
-                // of both column blocks
-                const int z0 = L - j * kKB;
-                for (int h = 0; h < 2; ++h)
-                    for (int e = z0 * 8 + lane; e < kKB * 8; e += 32)
-                        sts128(smem_u32(vs + h * kHalf + e * 16), 0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            const bool next = j + 1 < n;
-            if (next && !warp_wait(&k_full[s1], ((j + 1) / kStages) & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            for (int x = 0; x < kQT && ok; ++x) {
-                if (j >= qt[x].tiles) continue;
-                if (!warp_wait(&p_full[x], j & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
+            for (int j = 0; ok && j < n; ++j) {
+                const int s = j % kStages, s1 = (j + 1) % kStages;
+                const bool next = j + 1 < n;
+                ok = (j == n - 1 && tail) ? mbar_wait(v_tail, 0, abort)
+                                          : mbar_wait(&v_full[s], (j / kStages) & 1u, abort);
+                if (ok && next) ok = mbar_wait(&k_full[s1], ((j + 1) / kStages) & 1u, abort);
+                for (int x = 0; x < kQT && ok; ++x) {
+                    if (j >= qt[x].tiles) continue;
+                    ok = mbar_wait(&p_full[x], j & 1u, abort);
+                    if (!ok) break;
+                    tc_fence_after();
                     issue_pv(x, s, j > 0);
                     if (j + 1 < qt[x].tiles) issue_s(x, s1);
                 }
-                __syncwarp();
-            }
-            if (!ok) break;
-            if (lane == 0) {
-                umma_commit(&v_empty[s]);  // after both Q tiles' products with V_j
+                if (!ok) break;
+                umma_commit(&v_empty[s]);             // after both Q tiles' products with V_j
                 if (next) umma_commit(&k_empty[s1]);  // after both Q tiles' scores with K_j+1
             }
-            __syncwarp();
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         // arrives once every MMA issued has completed (TMEM is freed after it)
         if (lane == 0) umma_commit(mma_done);
     } else {
