@@ -52,7 +52,8 @@ constexpr int kQT = 2;                   // Q tiles per CTA
 constexpr int kKB = 128;                 // KV tokens per tile: two pages
 constexpr int kHalf = 128 * 128;         // 128 rows x 64 BF16: one 128-byte column block
 constexpr int kTileBytes = 2 * kHalf;    // a 128 x 128 BF16 tile (Q, K or V)
-constexpr int kStages = 2;               // K ring and V ring depth
+constexpr int kKStages = 2;              // K ring depth
+constexpr int kVStages = 2;              // V ring depth
 constexpr int kSoftmaxWarps = 4 * kQT;
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
@@ -63,13 +64,14 @@ constexpr float kRescaleLog2 = 8.f;      // P <= 2^8 between reference moves
 // Shared-memory layout (offsets from the 1024-byte aligned base).
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQT * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
 // p_full[2], o_done[2], mma_done, v_tail
-constexpr int kNumBars = 1 + 4 * kStages + 3 * kQT + 2;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kQT + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort word
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory over the per-CTA limit");
 
 struct PrefillArgs {
     const int32_t *seqlens;
@@ -130,9 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *q_full = bars;
-    uint64_t *k_full = bars + 1, *k_empty = k_full + kStages;
-    uint64_t *v_full = k_empty + kStages, *v_empty = v_full + kStages;
-    uint64_t *s_full = v_empty + kStages;  // [x]: S_x complete (and every MMA before it)
+    uint64_t *k_full = bars + 1, *k_empty = k_full + kKStages;
+    uint64_t *v_full = k_empty + kKStages, *v_empty = v_full + kVStages;
+    uint64_t *s_full = v_empty + kVStages;  // [x]: S_x complete (and every MMA before it)
     uint64_t *p_full = s_full + kQT;       // [x]: P_x written (four warps)
     uint64_t *o_done = p_full + kQT;       // [x]: O_x += P_x V complete
     uint64_t *mma_done = o_done + kQT;
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool tail = n > 0 && n * kKB > L;   // the last tile holds slots past L_r
 
     bool ok = true;
-    int q_issued = 0, k_issued[kStages] = {}, v_issued[kStages] = {};
+    int q_issued = 0, k_issued[kKStages] = {}, v_issued[kVStages] = {};
 
     if (warp == kProducerWarp) {
         const uint64_t pol = policy_evict_normal();
@@ -220,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool l1 = has1 && p1 >= 0 && p1 < a.num_pages;
                 if ((!l0 || (has1 && !l1)) && a.flags) atomicOr(a.flags, (int)HPC_FLAG_BAD_PAGE);
                 const uint32_t bytes = (uint32_t)((l0 ? 1 : 0) + (l1 ? 1 : 0)) * 2 * kTile * 128;
-                const int s = j % kStages;
-                const uint32_t par = ((j / kStages) & 1u) ^ 1u;
                 for (int kv = 0; kv < 2 && good; ++kv) {
+                    const int st = kv == 0 ? kKStages : kVStages, s = j % st;
+                    const uint32_t par = ((j / st) & 1u) ^ 1u;
                     uint64_t *full = kv == 0 ? &k_full[s] : &v_full[s];
                     if (!mbar_wait(kv == 0 ? &k_empty[s] : &v_empty[s], par, abort)) {
                         good = 0;
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tokens past L_r (the last page's free slots, or a page the
             // request does not have) must not reach P V: once the last V
             // tile has landed, zero those rows of both column blocks
-            const int jl = n - 1, s = jl % kStages;
-            if (!warp_wait(&v_full[s], (jl / kStages) & 1u, abort)) {
+            const int jl = n - 1, s = jl % kVStages;
+            if (!warp_wait(&v_full[s], (jl / kVStages) & 1u, abort)) {
                 ok = false;
             } else {
                 uint8_t *vs = smem + kOffV + s * kTileBytes;
@@ -308,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int j = 0; ok && j < n; ++j) {
-                const int s = j % kStages, s1 = (j + 1) % kStages;
+                const int s = j % kVStages, s1 = (j + 1) % kKStages;
                 const bool next = j + 1 < n;
                 ok = (j == n - 1 && tail) ? mbar_wait(v_tail, 0, abort)
-                                          : mbar_wait(&v_full[s], (j / kStages) & 1u, abort);
-                if (ok && next) ok = mbar_wait(&k_full[s1], ((j + 1) / kStages) & 1u, abort);
+                                          : mbar_wait(&v_full[s], (j / kVStages) & 1u, abort);
+                if (ok && next) ok = mbar_wait(&k_full[s1], ((j + 1) / kKStages) & 1u, abort);
                 for (int x = 0; x < kQT && ok; ++x) {
                     if (j >= qt[x].tiles) continue;
                     ok = mbar_wait(&p_full[x], j & 1u, abort);
@@ -438,10 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             drain(q_full, q_issued);
-            for (int s = 0; s < kStages; ++s) {
-                drain(&k_full[s], k_issued[s]);
-                drain(&v_full[s], v_issued[s]);
-            }
+            for (int s = 0; s < kKStages; ++s) drain(&k_full[s], k_issued[s]);
+            for (int s = 0; s < kVStages; ++s) drain(&v_full[s], v_issued[s]);
         }
     }
     tc_fence_before();

@@ -284,3 +284,25 @@ def test_multi_query_rows_match_full():
     full = run_mq(batch).reshape(-1, 128)
     rows = [0, 5, 17, 31, 47]
     assert np.array_equal(run_mq(batch, rows=rows), full[rows])
+
+
+# ------------------------------------------------------- extend / prefill
+# Many query tokens per request (the vLLM post's Table 4 prefill and extend
+# rows): the same rule at q_len in the hundreds, several 128-token query
+# blocks, prefills (L = q_len) and extends over a cached prefix.
+
+@pytest.mark.parametrize("q_len,lens", [(200, [200]), (130, [130, 400]), (300, [257, 300, 700])])
+def test_prefill_and_extend_match_library_sdpa_with_causal_mask(q_len, lens):
+    batch = mq_batch("bf16", q_len, lens, hq=4, hkv=2, seed=31)
+    got = run_mq(batch, num_threads=4)
+    ref = sdpa_causal_reference(batch)
+    assert np.allclose(got, ref, atol=1e-12, rtol=1e-10)
+
+
+def test_prefill_first_query_sees_only_the_first_token():
+    q_len = 150
+    batch = mq_batch("bf16", q_len, [q_len], hq=4, hkv=1, seed=33)
+    out = run_mq(batch, rows=[0, 1, 2, 3])  # query 0, every head
+    v0 = batch.v_cache.to(torch.float64)[int(batch.block_table[0, 0]), 0, 0].numpy()
+    for h in range(4):
+        assert np.array_equal(out[h], v0)
