@@ -98,6 +98,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                        uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -358,23 +365,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            for (int c = 0; c < 64; ++c) mx4[c & 3] = fmax3(mx4[c & 3], s[2 * c], s[2 * c + 1]);
+            const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
             const float m_tile = mx * sc;
             const bool need = m_tile > m_ref + kRescaleLog2;
             const float new_ref = need ? m_tile : m_ref;
             const float factor = need ? ex2(m_ref - new_ref) : 1.f;
             const float base = new_ref == -INFINITY ? 0.f : new_ref;
             float pk[64];  // P as packed BF16 pairs (bit patterns)
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 ps[4] = {};
+            const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-base, -base);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2(fmaf(s[2 * c], sc, -base));
-                const float p1 = ex2(fmaf(s[2 * c + 1], sc, -base));
-                ps[c & 3] += p0 + p1;
+            for (int c = 0; c < 64; ++c) {  // paired FP32 arithmetic: two columns per instruction
+                const float2 e = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
+                const float p0 = ex2(e.x), p1 = ex2(e.y);
+                ps[c & 3] = __fadd2_rn(ps[c & 3], make_float2(p0, p1));
                 pk[c] = __uint_as_float(pack_bf16x2(p0, p1));
             }
-            l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+            const float2 pq = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
+            l = l * factor + (pq.x + pq.y);
             // O_x is settled: its product with the previous tile completed
             // before these scores did
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
