@@ -12,8 +12,9 @@ and the output copied out inside the timed region; `cpu_baseline` is the fp64
 oracle timed on a bounded sample on the host cores; `static` is the in-house
 static split-KV schedule on the same batch.  Side legs: the fused prologue
 (`rope_norm`), multi-query decode (`mtp`), the router GEMM sweep
-(`router_gemm`) and extend / prefill attention on the vLLM comparison's
-shapes (`prefill`, TFLOP/s against the measured BF16 tensor peak).  Under
+(`router_gemm`), extend / prefill attention on the vLLM comparison's
+shapes (`prefill`, TFLOP/s against the measured BF16 tensor peak) and that
+table's decode rows (`table4_decode`, with the best static split-KV).  Under
 torchrun every rank runs an independent replica (the path has no exchange
 step).
 """
@@ -276,6 +277,7 @@ def parse_args():
     ap.add_argument("--no-mtp", action="store_true")
     ap.add_argument("--no-router", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-table4-decode", action="store_true")
     ap.add_argument("--prefill-shapes", default="",
                     help="comma-separated prefill/extend workloads (default: all of Table 4's)")
     ap.add_argument("--floor", type=int, default=None)
@@ -742,6 +744,48 @@ def main():
                    "peak_bf16_tflops": tf_peak, "peak_kind": tf_kind,
                    "l2": "flushed before every call", "shapes": rows}
 
+    # ---- the decode rows of the vLLM comparison's Table 4 at the same head
+    # shape: the whole step (assign + attention with the fused combine), and
+    # the best static split-KV step of a small sweep, L2 flushed before each
+    table4_decode = None
+    if not args.no_table4_decode:
+        from load_balanced_paged_assign_gb300.workloads import TABLE4_DECODE
+        rows = []
+        n_d = min(args.steps, 300)
+        bf16_ctas = hd.hpc_decode_num_ctas(local, hd.HPC_KV_BF16)
+        for name in TABLE4_DECODE:
+            wd = WORKLOADS[name]
+            bd = make_batch(wd, device=dev)
+            Bd, Hqd, Hkvd = wd.batch, wd.num_q_heads, wd.num_kv_heads
+            lens_d = bd.seqlens.cpu().tolist()
+
+            def dstep(w_s, S=0, bd=bd, wd=wd):
+                hd.hpc_decode_step(bd.q, bd.q_scale, bd.k_cache, bd.v_cache, bd.k_scale,
+                                   bd.v_scale, bd.block_table, bd.seqlens, wd.num_q_heads,
+                                   wd.num_kv_heads, wd.sm_scale, bf16_ctas, wd.min_tiles, S,
+                                   w_s.tmap, w_s.part_o, w_s.part_lse, w_s.out,
+                                   unit_done=w_s.unit_done)
+
+            wsd = hd.Workspace(Bd, Hqd, Hkvd, num_ctas=bf16_ctas, device=dev)
+            us = statistics.fmean(timed(n_d, args.warmup, lambda: dstep(wsd)))
+            md = hd.hpc_decode_read_meta(wsd.tmap)
+            if md[3] != 0:
+                raise RuntimeError(f"device error flags {md[3]}")
+            cnt = wsd.tmap.chunk_count[:Bd * Hkvd].tolist()
+            nb_d = algorithmic_bytes(lens_d, Hqd, Hkvd, "bf16", md[2], sum(c for c in cnt if c > 1))
+            st = {}
+            for S in (1, 2, 4, 8, 16):
+                sw = hd.Workspace(Bd, Hqd, Hkvd, num_splits=S, device=dev)
+                st[S] = statistics.fmean(timed(min(n_d, 100), 5, lambda sw=sw, S=S: dstep(sw, S)))
+            best = min(st, key=st.get)
+            rows.append({"workload": name, "batch": Bd, "seqlen": lens_d[0], "us_per_step": us,
+                         "gbps": nb_d["step"] / (us * 1e-6) / 1e9,
+                         "frac": nb_d["step"] / (us * 1e-6) / 1e9 / peak,
+                         "best_static_splits": best, "best_static_us": st[best],
+                         "dynamic_speedup_vs_best_static": st[best] / us})
+            del bd, wsd
+        table4_decode = {"heads": "Hq=64, Hkv=8, head_dim 128, BF16", "shapes": rows}
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
@@ -777,6 +821,7 @@ def main():
         "mtp": mtp,
         "router_gemm": router,
         "prefill": prefill,
+        "table4_decode": table4_decode,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
     }

@@ -123,6 +123,21 @@ for _i, (_name, (_b, _q, _l)) in enumerate(TABLE4_PREFILL.items()):
                                             f"Hkv=8, BF16")
 
 
+# The decode rows of the same table ("Bq1sL": batch B, one query token, KV
+# length L), at the same head shape.  The H20 latencies fit it: 64q1s4k moves
+# 1.07 GB of BF16 KV in 0.299 ms (~3.6 TB/s on a 4 TB/s part).
+TABLE4_DECODE = {
+    "t4_8q1s1k": (8, 1024),
+    "t4_16q1s2k": (16, 2048),
+    "t4_32q1s1k": (32, 1024),
+    "t4_64q1s4k": (64, 4096),
+}
+for _i, (_name, (_b, _l)) in enumerate(TABLE4_DECODE.items()):
+    WORKLOADS[_name] = Workload(_name, _b, 64, 8, draw=((_b, "fixed", _l, _l),), seed=1400 + _i,
+                                description=f"Table-4 decode {_name[3:]}: B={_b}, L={_l}, Hq=64, "
+                                            f"Hkv=8, BF16")
+
+
 def draw_seqlens(w: Workload, gen: torch.Generator) -> list:
     if w.seqlens:
         return [int(x) for x in w.seqlens]

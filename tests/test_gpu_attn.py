@@ -331,3 +331,20 @@ def test_randomized_stress_against_oracle():
         b, _ = run_step(batch, num_ctas=ctas, floor=floor, fused=fused)
         assert torch.equal(a, b), f"case {case} not deterministic"
         assert_close(a, oracle_out(batch), kv_dtype)
+
+
+@pytest.mark.parametrize("name", ["t4_8q1s1k", "t4_16q1s2k", "t4_32q1s1k", "t4_64q1s4k"])
+def test_table4_decode_rows(name):
+    """The decode rows of the vLLM comparison's Table 4 (Hq = 64, Hkv = 8):
+    the task map bit-exact against the oracle, outputs on sampled rows, the
+    dynamic and the static schedule."""
+    w = WORKLOADS[name]
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), w.num_kv_heads, device_ctas("bf16"),
+                       w.min_tiles)
+    rows = sample_rows(batch, 96, 5, list(range(64)))
+    ref = oracle_out(batch, rows=rows)
+    assert_close(out, ref, "bf16", rows=rows)
+    static, _ = run_step(batch, num_splits=4)
+    assert_close(static, ref, "bf16", rows=rows)
