@@ -226,3 +226,28 @@ def test_router_argument_checks(hd):
     assert L.hpc_router_split(FAKE, 0, 4096, FAKE, FAKE, None) == E.HPC_ERR_ARG
     assert L.hpc_router_workspace_bytes(4, 192, 4000) == -1
     assert L.hpc_router_workspace_bytes(0, 192, 4096) == 0
+
+
+def test_prefill_argument_checks(hd):
+    L = hd.lib()
+    E = hd.binding
+
+    def call(q=FAKE, k=FAKE, v=FAKE, num_pages=100, bt=FAKE, max_pages=8, sl=FAKE, B=2, Hq=8,
+             Hkv=2, D=128, q_len=300, sm=0.088, out=FAKE):
+        return L.hpc_prefill_attn(q, k, v, num_pages, bt, max_pages, sl, B, Hq, Hkv, D, q_len,
+                                  sm, out, None, None)
+
+    assert call(B=0) == E.HPC_OK  # nothing to do, nothing launched
+    assert call(D=64) == E.HPC_ERR_UNSUPPORTED
+    assert call(Hq=6, Hkv=4) == E.HPC_ERR_UNSUPPORTED
+    assert call(q_len=0) == E.HPC_ERR_ARG
+    assert call(B=-1) == E.HPC_ERR_ARG
+    assert call(num_pages=0) == E.HPC_ERR_ARG
+    assert call(max_pages=0) == E.HPC_ERR_ARG
+    assert call(q=None) == E.HPC_ERR_ARG
+    assert call(out=None) == E.HPC_ERR_ARG
+    assert call(sl=None) == E.HPC_ERR_ARG
+    assert call(q=FAKE + 8) == E.HPC_ERR_ARG  # not 16-byte aligned
+    assert call(k=FAKE + 4) == E.HPC_ERR_ARG
+    assert call(sm=float("inf")) == E.HPC_ERR_ARG
+    assert call(max_pages=1 << 24) == E.HPC_ERR_UNSUPPORTED  # token index past int32 range
