@@ -389,18 +389,22 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
 
 // Merge of split unit `di` for query row rho (= i * G + g) by one warp: lane l
 // owns dims 4l .. 4l + 3; LSEs are read lane-parallel and their weights
-// broadcast by shuffle, with eight partial rows in flight at a time.  A row
-// that sees no token in any chunk (multi-query rows of a request shorter
-// than q_len) is written as zeros.
+// broadcast by shuffle, with MB partial rows in flight at a time (the merge
+// runs at the end of the stream, when the registers are free, so a long
+// unit's chunks cost few L2 round trips; MB = 16 for one row block, 8 for two,
+// whose kernels have fewer registers to spare).  A row that sees no token in
+// any chunk (multi-query rows of a request shorter than q_len) is written as
+// zeros.
+template <int MB>
 __device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescInfo &di, int rho) {
     const int lane = threadIdx.x & 31;
     const float *lse = p.part_lse + (size_t)di.chunk_off * p.R + rho;
     const float4 *po = reinterpret_cast<const float4 *>(
                            p.part_o + ((size_t)di.chunk_off * p.R + rho) * kHeadDim) + lane;
     const size_t row = (size_t)p.R * kHeadDim / 4;  // float4s between chunk rows
-    float4 x[8];
+    float4 x[MB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < MB; ++j)
         x[j] = j < di.count ? __ldcg(po + (size_t)j * row) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float lv0 = lane < di.count ? __ldcg(lse + (size_t)lane * p.R) : kNegInf;
     float m = lv0;
@@ -418,15 +422,15 @@ __device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescI
 #pragma unroll
         for (int o_ = 16; o_ > 0; o_ >>= 1) ws += __shfl_xor_sync(kFullMask, ws, o_);
         wsum += ws;
-        for (int i0 = 0; i0 < cnt; i0 += 8) {
+        for (int i0 = 0; i0 < cnt; i0 += MB) {
             if (base | i0) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < MB; ++j)
                     x[j] = i0 + j < cnt ? __ldcg(po + (size_t)(base + i0 + j) * row)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < MB; ++j) {
                 const float w = __shfl_sync(kFullMask, wl, (i0 + j) & 31);
                 acc.x += w * x[j].x; acc.y += w * x[j].y;
                 acc.z += w * x[j].z; acc.w += w * x[j].w;
@@ -582,7 +586,7 @@ __device__ __forceinline__ bool attn_combiner(const AttnParams &p, uint8_t *smem
                         if (lane == 0) last[1 + nlast].di = di;
                         ++nlast;
                     } else {  // list full (many bins per CTA): merge here, alone
-                        for (int rho = 0; rho < p.R; ++rho) merge_unit_head(p, di, rho);
+                        for (int rho = 0; rho < p.R; ++rho) merge_unit_head<NB == 1 ? 16 : 8>(p, di, rho);
                     }
                 }
             }
@@ -955,7 +959,7 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
     const int nlast = last[0].flags;
     const int nw = 1 + Tr::kConsumers, w = warp - 1;
     for (int item = w; item < nlast * p.R; item += nw)
-        merge_unit_head(p, last[1 + item / p.R].di, item % p.R);
+        merge_unit_head<NB == 1 ? 16 : 8>(p, last[1 + item / p.R].di, item % p.R);
 }
 
 }  // namespace hpc
