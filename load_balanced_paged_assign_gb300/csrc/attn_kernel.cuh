@@ -447,6 +447,68 @@ __device__ __forceinline__ void merge_unit_head(const AttnParams &p, const DescI
         make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
+// The same for K rows at once (rows of split units with at most 32 chunks):
+// each round issues MB partial rows of every one of the K rows before any is
+// consumed, so a warp merging two rows pays the L2 round trips once.
+template <int MB, int K>
+__device__ __forceinline__ void merge_unit_rows(const AttnParams &p, const DescInfo (&di)[K],
+                                                const int (&rho)[K]) {
+    const int lane = threadIdx.x & 31;
+    const size_t row = (size_t)p.R * kHeadDim / 4;  // float4s between chunk rows
+    const float4 *po[K];
+    float wl[K], wsum[K], m[K];
+    float4 acc[K];
+    int maxc = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        po[k] = reinterpret_cast<const float4 *>(p.part_o +
+                                                 ((size_t)di[k].chunk_off * p.R + rho[k]) * kHeadDim) +
+                lane;
+        const float *lse = p.part_lse + (size_t)di[k].chunk_off * p.R + rho[k];
+        wl[k] = lane < di[k].count ? __ldcg(lse + (size_t)lane * p.R) : kNegInf;
+        maxc = max(maxc, di[k].count);
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        m[k] = wl[k];
+#pragma unroll
+        for (int o_ = 16; o_ > 0; o_ >>= 1) m[k] = fmaxf(m[k], __shfl_xor_sync(kFullMask, m[k], o_));
+        wl[k] = lane < di[k].count ? ex2((wl[k] - m[k]) * kLog2e) : 0.f;
+        wsum[k] = wl[k];
+#pragma unroll
+        for (int o_ = 16; o_ > 0; o_ >>= 1) wsum[k] += __shfl_xor_sync(kFullMask, wsum[k], o_);
+    }
+    for (int i0 = 0; i0 < maxc; i0 += MB) {
+        float4 x[K][MB];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < MB; ++j)
+                x[k][j] = i0 + j < di[k].count ? __ldcg(po[k] + (size_t)(i0 + j) * row)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < MB; ++j) {
+                const float w = __shfl_sync(kFullMask, wl[k], (i0 + j) & 31);
+                acc[k].x += w * x[k][j].x; acc[k].y += w * x[k][j].y;
+                acc[k].z += w * x[k][j].z; acc[k].w += w * x[k][j].w;
+            }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float inv = m[k] == kNegInf ? 0.f : 1.f / wsum[k];
+        const float4 a = inv == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f) : acc[k];
+        const int qi = rho[k] / p.G;
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) +
+                             (((size_t)di[k].req * p.q_len + qi) * p.Hq + di[k].kv_head * p.G +
+                              (rho[k] - qi * p.G)) * kHeadDim + 4 * lane;
+        *reinterpret_cast<uint2 *>(dst) =
+            make_uint2(pack_bf16x2(a.x * inv, a.y * inv), pack_bf16x2(a.z * inv, a.w * inv));
+    }
+}
+
 // ------------------------------------------------------------------ combiner
 // Register r = 4 j + e of accumulator lane (g, t4) holds (dim, head):
 //   head = 2 t4 + (e & 1);
@@ -958,8 +1020,31 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
     const SlotInfo *last = reinterpret_cast<const SlotInfo *>(smem + Tr::kOffLast);
     const int nlast = last[0].flags;
     const int nw = 1 + Tr::kConsumers, w = warp - 1;
-    for (int item = w; item < nlast * p.R; item += nw)
-        merge_unit_head<NB == 1 ? 16 : 8>(p, last[1 + item / p.R].di, item % p.R);
+    const int items = nlast * p.R;
+    if constexpr (!FP8 && NB == 1) {
+        // BF16 decode: five merging warps, so a unit's eight rows take two
+        // passes one row at a time; two rows per warp, their loads in flight
+        // together, take one
+        for (int item = 2 * w; item < items; item += 2 * nw) {
+            const DescInfo &d0 = last[1 + item / p.R].di;
+            if (item + 1 < items) {
+                const DescInfo &d1 = last[1 + (item + 1) / p.R].di;
+                if (d0.count <= 32 && d1.count <= 32) {
+                    const DescInfo dd[2] = {d0, d1};
+                    const int rr[2] = {item % p.R, (item + 1) % p.R};
+                    merge_unit_rows<8, 2>(p, dd, rr);
+                } else {
+                    merge_unit_head<16>(p, d0, item % p.R);
+                    merge_unit_head<16>(p, d1, (item + 1) % p.R);
+                }
+            } else {
+                merge_unit_head<16>(p, d0, item % p.R);
+            }
+        }
+    } else {
+        for (int item = w; item < items; item += nw)
+            merge_unit_head<NB == 1 ? 16 : 8>(p, last[1 + item / p.R].di, item % p.R);
+    }
 }
 
 }  // namespace hpc
