@@ -1021,10 +1021,10 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
     const int nlast = last[0].flags;
     const int nw = 1 + Tr::kConsumers, w = warp - 1;
     const int items = nlast * p.R;
-    if constexpr (!FP8 && NB == 1) {
-        // BF16 decode: five merging warps, so a unit's eight rows take two
-        // passes one row at a time; two rows per warp, their loads in flight
-        // together, take one
+    if constexpr (!FP8) {
+        // BF16: five merging warps, so a unit's eight rows (sixteen with two
+        // query tokens) take two (four) passes one row at a time; two rows per
+        // warp, their loads in flight together, take half as many
         for (int item = 2 * w; item < items; item += 2 * nw) {
             const DescInfo &d0 = last[1 + item / p.R].di;
             if (item + 1 < items) {
@@ -1034,11 +1034,11 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
                     const int rr[2] = {item % p.R, (item + 1) % p.R};
                     merge_unit_rows<8, 2>(p, dd, rr);
                 } else {
-                    merge_unit_head<16>(p, d0, item % p.R);
-                    merge_unit_head<16>(p, d1, (item + 1) % p.R);
+                    merge_unit_head<NB == 1 ? 16 : 8>(p, d0, item % p.R);
+                    merge_unit_head<NB == 1 ? 16 : 8>(p, d1, (item + 1) % p.R);
                 }
             } else {
-                merge_unit_head<16>(p, d0, item % p.R);
+                merge_unit_head<NB == 1 ? 16 : 8>(p, d0, item % p.R);
             }
         }
     } else {
