@@ -502,19 +502,42 @@ def main():
     unf = graphed(lambda: step(ws, fused=False)) if args.graph else (lambda: step(ws, fused=False))
     unfused_us = statistics.fmean(timed(n_unf, args.warmup, unf))
 
-    # ---- e2e: the same step through the host-buffer C entry point
+    # ---- e2e: the same step through the host-buffer C entry points: the
+    # step's inputs packed in one pinned host buffer (one copy in, one out),
+    # and for context the separate-buffer call (one copy per input array)
     e2e = None
     if not args.no_e2e:
+        kvd = hd.HPC_KV_FP8_E4M3 if fp8 else hd.HPC_KV_BF16
+        total, off = hd.hpc_decode_packed_layout(B, Hq, batch.max_pages, kvd)
+        h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+
+        def put(o, t):
+            raw = t.cpu().contiguous().view(torch.uint8).reshape(-1)
+            h_in[o:o + raw.numel()] = raw
+
+        put(off[0], batch.q)
+        if fp8:
+            put(off[1], batch.q_scale)
+        put(off[2], batch.seqlens)
+        put(off[3], batch.block_table)
+        d_in = torch.empty(total, dtype=torch.uint8, device=dev)
+        h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            hd.hpc_decode_step_host_packed(h_in, d_in, h_out, ws.out, batch.k_cache, batch.v_cache,
+                                           batch.k_scale, batch.v_scale, B, Hq, Hkv,
+                                           batch.max_pages, w.sm_scale, ctas, floor, 0, ws.tmap,
+                                           ws.part_o, ws.part_lse, ws.unit_done)
+
         h_q = batch.q.cpu().pin_memory()
         h_qs = batch.q_scale.cpu().pin_memory() if fp8 else None
         h_sl = batch.seqlens.cpu().pin_memory()
         h_bt = batch.block_table.cpu().pin_memory()
-        h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
         d_q, d_sl, d_bt = (torch.empty_like(batch.q), torch.empty_like(batch.seqlens),
                            torch.empty_like(batch.block_table))
         d_qs = torch.empty_like(batch.q_scale) if fp8 else None
 
-        def e2e_step():
+        def e2e_step_separate():
             hd.hpc_decode_step_host(h_q, h_qs, h_sl, h_bt, h_out, d_q, d_qs, d_sl, d_bt, ws.out,
                                     batch.k_cache, batch.v_cache, batch.k_scale, batch.v_scale,
                                     Hq, Hkv, w.sm_scale, ctas, floor, 0, ws.tmap, ws.part_o,
@@ -522,12 +545,13 @@ def main():
 
         n_e2e = min(args.steps, 1000)
         tot = timed(n_e2e, args.warmup, e2e_step)
-        h2d = (h_q.numel() * h_q.element_size() + h_sl.numel() * 4 + h_bt.numel() * 4 +
-               (h_qs.numel() * 4 if fp8 else 0))
+        sep = timed(n_e2e, args.warmup, e2e_step_separate)
         d2h = h_out.numel() * 2
         e2e = {"value": max(max_over_ranks(statistics.fmean(tot), world)), "unit": "us/step",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "api": "hpc_decode_step_host (pinned host buffers)"}
+               "h2d_bytes_per_step": total, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "api": "hpc_decode_step_host_packed (one pinned input buffer, one copy each way)",
+               "separate_buffers_us": statistics.fmean(sep),
+               "separate_buffers_api": "hpc_decode_step_host (a copy per input array)"}
 
     # ---- in-house static split-KV comparator on the same batch
     static = None

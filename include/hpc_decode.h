@@ -343,6 +343,35 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
                                 int32_t *d_unit_done, hpc_stream_t stream);
 
 /*
+ * Layout of the packed per-step input of hpc_decode_step_host_packed: one
+ * buffer holding the query, the FP8 query scales (FP8 only), the seqlens and
+ * the block table, each section starting on a 16-byte boundary.  Writes the
+ * byte offsets {q, q_scale (-1 for BF16), seqlens, block_table} to offsets[4]
+ * and returns the total size in bytes (-1 for invalid arguments).  Sections
+ * are laid out exactly as the separate arrays of hpc_decode_step.
+ */
+int64_t hpc_decode_packed_layout(int32_t B, int32_t Hq, int32_t max_pages_per_req,
+                                 hpc_kv_dtype kv_dtype, int64_t offsets[4]);
+
+/*
+ * hpc_decode_step_host with the per-step inputs in ONE host buffer h_in
+ * (the layout of hpc_decode_packed_layout; pinned memory makes the copy
+ * asynchronous): one host-to-device copy into the caller's device staging
+ * buffer d_in (same size, 16-byte aligned), the step on the device sections,
+ * and one device-to-host copy of d_out into h_out.  The same bytes move as
+ * with the separate buffers, in one transfer each way.
+ */
+hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out, void *d_out,
+                                       const void *d_k_cache, const void *d_v_cache,
+                                       int32_t num_pages, float k_scale, float v_scale,
+                                       hpc_kv_dtype kv_dtype, int32_t max_pages_per_req,
+                                       int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                       float sm_scale, int32_t num_ctas,
+                                       int32_t min_tiles_per_cta, int32_t num_splits,
+                                       hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                                       int32_t *d_unit_done, hpc_stream_t stream);
+
+/*
  * Size of the scratch array compiled into the library for
  * hpc_decode_step_noalloc.
  */

@@ -17,7 +17,8 @@ from .binding import (EXPORTS, HPC_KV_BF16, HPC_KV_FP8_E4M3, HPC_ROPE_HALVES,
                       hpc_decode_num_ctas, hpc_decode_plan, hpc_decode_plan_static,
                       hpc_decode_read_meta, hpc_decode_static_capacity, hpc_decode_step,
                       hpc_decode_step_mq,
-                      hpc_decode_step_host, hpc_decode_version, hpc_prefill_attn,
+                      hpc_decode_packed_layout, hpc_decode_step_host,
+                      hpc_decode_step_host_packed, hpc_decode_version, hpc_prefill_attn,
                       hpc_rope_frequencies, hpc_rope_norm, hpc_router_gemm, hpc_router_split, hpc_router_workspace_bytes,
                       kv_dtype_of, lib)
 
@@ -27,7 +28,8 @@ __all__ = [
     "hpc_decode_attn_combine_mq", "hpc_decode_attn_mq", "hpc_decode_combine",
     "hpc_decode_combine_mq", "hpc_decode_desc_capacity", "hpc_decode_num_ctas",
     "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_read_meta",
-    "hpc_decode_static_capacity", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_step_mq",
+    "hpc_decode_packed_layout", "hpc_decode_static_capacity", "hpc_decode_step",
+    "hpc_decode_step_host", "hpc_decode_step_host_packed", "hpc_decode_step_mq",
     "hpc_decode_version", "hpc_prefill_attn", "hpc_rope_frequencies", "hpc_rope_norm", "hpc_router_gemm",
     "hpc_router_split", "hpc_router_workspace_bytes", "kv_dtype_of", "lib",
 ]

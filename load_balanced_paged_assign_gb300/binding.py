@@ -29,6 +29,7 @@ EXPORTS = (
     "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
     "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
     "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_gemm", "hpc_prefill_attn",
+    "hpc_decode_packed_layout", "hpc_decode_step_host_packed",
 )
 
 
@@ -107,6 +108,11 @@ def lib():
         "hpc_router_gemm": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
         "hpc_prefill_attn": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                             i32, f32, vp, vp, vp]),
+        "hpc_decode_packed_layout": (i64, [i32, i32, i32, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_int64)]),
+        "hpc_decode_step_host_packed": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, f32, f32,
+                                                       ctypes.c_int, i32, i32, i32, i32, i32, f32,
+                                                       i32, i32, i32, tm, vp, vp, vp, vp]),
         "hpc_decode_attn_mq": (ctypes.c_int, [vp, vp, vp, vp, i32, f32, f32, ctypes.c_int, vp,
                                               i32, vp, i32, i32, i32, i32, i32, f32, tm, vp, vp,
                                               vp]),
@@ -362,6 +368,30 @@ def hpc_decode_step_host(h_q, h_q_scale, h_seqlens, h_block_table, h_out, d_q, d
         int(Hkv), HEAD_DIM, float(sm_scale), int(num_ctas), int(min_tiles_per_cta),
         int(num_splits), ctypes.byref(tmap.c), _ptr(part_o), _ptr(part_lse), _ptr(unit_done),
         _stream(stream)))
+
+
+def hpc_decode_packed_layout(B, Hq, max_pages, kv_dtype=HPC_KV_BF16):
+    """(total bytes, [q, q_scale or -1, seqlens, block_table] byte offsets) of the
+    packed per-step input."""
+    off = (ctypes.c_int64 * 4)()
+    total = int(lib().hpc_decode_packed_layout(int(B), int(Hq), int(max_pages), int(kv_dtype),
+                                                 off))
+    if total < 0:
+        raise HpcError("hpc_decode_packed_layout", HPC_ERR_ARG)
+    return total, list(off)
+
+
+def hpc_decode_step_host_packed(h_in, d_in, h_out, d_out, k_cache, v_cache, k_scale, v_scale, B,
+                                Hq, Hkv, max_pages, sm_scale, num_ctas, min_tiles_per_cta,
+                                num_splits, tmap: TaskMap, part_o, part_lse, unit_done=None,
+                                stream=None):
+    """One decode step from one packed pinned host buffer (see hpc_decode_packed_layout)."""
+    _check("hpc_decode_step_host_packed", lib().hpc_decode_step_host_packed(
+        _ptr(h_in), _ptr(d_in), _ptr(h_out), _ptr(d_out), _ptr(k_cache), _ptr(v_cache),
+        int(k_cache.shape[0]), float(k_scale), float(v_scale), kv_dtype_of(k_cache),
+        int(max_pages), int(B), int(Hq), int(Hkv), HEAD_DIM, float(sm_scale), int(num_ctas),
+        int(min_tiles_per_cta), int(num_splits), ctypes.byref(tmap.c), _ptr(part_o),
+        _ptr(part_lse), _ptr(unit_done), _stream(stream)))
 
 
 def hpc_decode_read_meta(tmap: TaskMap, stream=None) -> list:

@@ -516,6 +516,56 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
     return cuda_status(e);
 }
 
+int64_t hpc_decode_packed_layout(int32_t B, int32_t Hq, int32_t max_pages_per_req,
+                                 hpc_kv_dtype kv_dtype, int64_t offsets[4]) {
+    if (B < 0 || Hq <= 0 || max_pages_per_req <= 0 || !offsets) return -1;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return -1;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    auto up16 = [](int64_t x) { return (x + 15) & ~int64_t(15); };
+    int64_t off = 0;
+    offsets[0] = off;
+    off = up16(off + (int64_t)B * Hq * HPC_HEAD_DIM * (fp8 ? 1 : 2));
+    offsets[1] = fp8 ? off : -1;
+    if (fp8) off = up16(off + (int64_t)B * Hq * 4);
+    offsets[2] = off;
+    off = up16(off + (int64_t)B * 4);
+    offsets[3] = off;
+    off = up16(off + (int64_t)B * max_pages_per_req * 4);
+    return off;
+}
+
+hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out, void *d_out,
+                                       const void *d_k_cache, const void *d_v_cache,
+                                       int32_t num_pages, float k_scale, float v_scale,
+                                       hpc_kv_dtype kv_dtype, int32_t max_pages_per_req,
+                                       int32_t B, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                       float sm_scale, int32_t num_ctas,
+                                       int32_t min_tiles_per_cta, int32_t num_splits,
+                                       hpc_task_map *map, float *d_part_o, float *d_part_lse,
+                                       int32_t *d_unit_done, hpc_stream_t stream) {
+    hpc_status st = check_shapes(B, Hq, Hkv, head_dim, max_pages_per_req);
+    if (st != HPC_OK) return st;
+    int64_t off[4];
+    const int64_t bytes = hpc_decode_packed_layout(B, Hq, max_pages_per_req, kv_dtype, off);
+    if (bytes < 0) return HPC_ERR_ARG;
+    if (B > 0 && (!h_in || !d_in || !h_out || !d_out)) return HPC_ERR_ARG;
+    if (B > 0 && !aligned16(d_in)) return HPC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    char *d = static_cast<char *>(d_in);
+    if (B > 0 && cudaMemcpyAsync(d_in, h_in, (size_t)bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return HPC_ERR_CUDA;
+    st = hpc_decode_step(d + off[0], fp8 ? reinterpret_cast<const float *>(d + off[1]) : nullptr,
+                         d_k_cache, d_v_cache, num_pages, k_scale, v_scale, kv_dtype,
+                         reinterpret_cast<const int32_t *>(d + off[3]), max_pages_per_req,
+                         reinterpret_cast<const int32_t *>(d + off[2]), B, Hq, Hkv, head_dim,
+                         sm_scale, num_ctas, min_tiles_per_cta, num_splits, map, d_part_o,
+                         d_part_lse, d_unit_done, d_out, stream);
+    if (st != HPC_OK || B == 0) return st;
+    return cuda_status(cudaMemcpyAsync(h_out, d_out, (size_t)B * Hq * HPC_HEAD_DIM * 2,
+                                       cudaMemcpyDeviceToHost, s));
+}
+
 hpc_status hpc_decode_read_meta(const hpc_task_map *map, int32_t host_meta[4],
                                 hpc_stream_t stream) {
     if (!map || !map->meta || !host_meta) return HPC_ERR_ARG;

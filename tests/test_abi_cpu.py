@@ -251,3 +251,35 @@ def test_prefill_argument_checks(hd):
     assert call(k=FAKE + 4) == E.HPC_ERR_ARG
     assert call(sm=float("inf")) == E.HPC_ERR_ARG
     assert call(max_pages=1 << 24) == E.HPC_ERR_UNSUPPORTED  # token index past int32 range
+
+
+def test_packed_layout(hd):
+    E = hd.binding
+    total, off = hd.hpc_decode_packed_layout(32, 8, 512, E.HPC_KV_BF16)
+    assert off == [0, -1, 32 * 8 * 128 * 2, 32 * 8 * 128 * 2 + 128]
+    assert total == off[3] + 32 * 512 * 4
+    total, off = hd.hpc_decode_packed_layout(3, 8, 5, E.HPC_KV_FP8_E4M3)
+    assert off[0] == 0 and off[1] == 3 * 8 * 128 and off[2] == off[1] + 96
+    assert all(o % 16 == 0 for o in off) and total % 16 == 0
+    assert off[3] >= off[2] + 3 * 4 and total >= off[3] + 3 * 5 * 4
+    L = hd.lib()
+    o = (ctypes.c_int64 * 4)()
+    assert L.hpc_decode_packed_layout(-1, 8, 5, 0, o) == -1
+    assert L.hpc_decode_packed_layout(3, 8, 0, 0, o) == -1
+    assert L.hpc_decode_packed_layout(3, 8, 5, 7, o) == -1
+
+
+def test_packed_step_argument_checks(hd):
+    L = hd.lib()
+    E = hd.binding
+    m = E.hpc_task_map()
+
+    def call(h_in=FAKE, d_in=FAKE, h_out=FAKE, d_out=FAKE, B=4, D=128):
+        return L.hpc_decode_step_host_packed(h_in, d_in, h_out, d_out, FAKE, FAKE, 100, 1.0, 1.0,
+                                             0, 8, B, 8, 1, D, 0.088, 132, 2, 0,
+                                             ctypes.byref(m), FAKE, FAKE, FAKE, None)
+
+    assert call(h_in=None) == E.HPC_ERR_ARG
+    assert call(d_out=None) == E.HPC_ERR_ARG
+    assert call(d_in=FAKE + 8) == E.HPC_ERR_ARG  # device staging not 16-byte aligned
+    assert call(D=64) == E.HPC_ERR_UNSUPPORTED

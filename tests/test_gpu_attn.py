@@ -348,3 +348,33 @@ def test_table4_decode_rows(name):
     assert_close(out, ref, "bf16", rows=rows)
     static, _ = run_step(batch, num_splits=4)
     assert_close(static, ref, "bf16", rows=rows)
+
+
+@pytest.mark.parametrize("name", ["hy3_tp8", "fp8"])
+def test_packed_host_step_equals_the_device_step(name):
+    """hpc_decode_step_host_packed: one pinned input buffer, one copy each way;
+    the output is bit-identical to the device-buffer step on the same inputs."""
+    w = WORKLOADS[name]
+    batch = make_batch(w, device="cuda")
+    ref, _ = run_step(batch)
+    fp8 = w.kv_dtype == "e4m3"
+    B, Hq, Hkv, mp = w.batch, w.num_q_heads, w.num_kv_heads, batch.max_pages
+    kvd = hd.HPC_KV_FP8_E4M3 if fp8 else hd.HPC_KV_BF16
+    total, off = hd.hpc_decode_packed_layout(B, Hq, mp, kvd)
+    h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    h_in[off[0]:off[0] + batch.q.numel() * batch.q.element_size()] = \
+        batch.q.cpu().contiguous().view(torch.uint8).reshape(-1)
+    if fp8:
+        h_in[off[1]:off[1] + B * Hq * 4] = batch.q_scale.cpu().contiguous().view(torch.uint8).reshape(-1)
+    h_in[off[2]:off[2] + B * 4] = batch.seqlens.cpu().view(torch.uint8)
+    h_in[off[3]:off[3] + B * mp * 4] = batch.block_table.cpu().contiguous().view(torch.uint8).reshape(-1)
+    d_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    ctas = device_ctas(w.kv_dtype)
+    ws = hd.Workspace(B, Hq, Hkv, num_ctas=ctas, device="cuda", kv_dtype=kvd)
+    h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+    hd.hpc_decode_step_host_packed(h_in, d_in, h_out, ws.out, batch.k_cache, batch.v_cache,
+                                   batch.k_scale, batch.v_scale, B, Hq, Hkv, mp, w.sm_scale, ctas,
+                                   w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse,
+                                   unit_done=ws.unit_done)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out.view(torch.int16), ref.cpu().view(torch.int16))
