@@ -767,6 +767,37 @@ def main():
         prefill = {"heads": "Hq=64, Hkv=8, head_dim 128, BF16 (Hy3 TP1 shape)",
                    "peak_bf16_tflops": tf_peak, "peak_kind": tf_kind,
                    "l2": "flushed before every call", "shapes": rows}
+        # the fp64 oracle beside it (rank 0, one GPU): a bounded sample of one
+        # shape's query rows on the host cores, scaled to the whole shape by
+        # the causal (row, token) pairs it covers
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            import numpy as np
+
+            import oracle
+            name = "t4_q4k" if "t4_q4k" in shapes else shapes[-1]
+            wp = WORKLOADS[name]
+            bp = make_batch(wp, device="cpu")
+            Hqp, qn = wp.num_q_heads, wp.q_len
+            lens_p = bp.seqlens.tolist()
+            n_rows = len(lens_p) * qn * Hqp
+            rng = np.random.default_rng(7)
+            sample = np.sort(rng.choice(n_rows, min(n_rows, 4096), replace=False))
+
+            def visible(row):
+                rq, i = row // (qn * Hqp), (row // Hqp) % qn
+                return max(0, lens_p[rq] - qn + 1 + i)
+
+            t = time.perf_counter()
+            oracle.attention_mq(bp.q, bp.k_cache, bp.v_cache, bp.block_table, bp.seqlens, qn,
+                                rows=sample, **bp.oracle_kwargs())
+            dt = time.perf_counter() - t
+            pairs_sample = sum(visible(int(x)) for x in sample)
+            pairs_all = prefill_flops(lens_p, qn, Hqp) / (4 * 128)
+            prefill["cpu_baseline"] = {
+                "workload": name, "value": dt * pairs_all / max(pairs_sample, 1) * 1e6,
+                "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"{len(sample)} of {n_rows} query rows, fp64, scaled by causal pairs"}
+            del bp
 
     # ---- the decode rows of the vLLM comparison's Table 4 at the same head
     # shape: the whole step (assign + attention with the fused combine), and
