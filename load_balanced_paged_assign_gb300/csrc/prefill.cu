@@ -355,32 +355,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            // the row's 128 scores in two halves: the second half loads while
+            // the first is masked and reduced
+            uint32_t ra[32], rb[32], rc[32], rd[32];
+            tmem_ld32_nowait(scol, ra);
+            tmem_ld32_nowait(scol + 32, rb);
+            tmem_wait_ld32x2(ra, rb);
+            tmem_ld32_nowait(scol + 64, rc);
+            tmem_ld32_nowait(scol + 96, rd);
             float s[128];
-            tmem_ld32x2(scol, scol + 32, *reinterpret_cast<float(*)[64]>(s));
-            tmem_ld32x2(scol + 64, scol + 96, *reinterpret_cast<float(*)[64]>(s + 64));
-            if (j * kKB + kKB - 1 > t.lim_first) {  // the causal diagonal or the request's end
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < 32; ++c) {
+                s[c] = __uint_as_float(ra[c]);
+                s[32 + c] = __uint_as_float(rb[c]);
+            }
+            const bool diag = j * kKB + kKB - 1 > t.lim_first;  // the causal diagonal or the end
+            if (diag) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
                     if (j * kKB + c > lim) s[c] = -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx4[c & 3] = fmax3(mx4[c & 3], s[2 * c], s[2 * c + 1]);
+            for (int c = 0; c < 32; ++c) mx4[c & 3] = fmax3(mx4[c & 3], s[2 * c], s[2 * c + 1]);
+            tmem_wait_ld32x2(rc, rd);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                s[64 + c] = __uint_as_float(rc[c]);
+                s[96 + c] = __uint_as_float(rd[c]);
+            }
+            if (diag) {
+#pragma unroll
+                for (int c = 64; c < 128; ++c)
+                    if (j * kKB + c > lim) s[c] = -INFINITY;
+            }
+#pragma unroll
+            for (int c = 32; c < 64; ++c) mx4[c & 3] = fmax3(mx4[c & 3], s[2 * c], s[2 * c + 1]);
             const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
             const float m_tile = mx * sc;
             const bool need = m_tile > m_ref + kRescaleLog2;
             const float new_ref = need ? m_tile : m_ref;
             const float factor = need ? ex2(m_ref - new_ref) : 1.f;
             const float base = new_ref == -INFINITY ? 0.f : new_ref;
-            float pk[64];  // P as packed BF16 pairs (bit patterns)
+            // P as packed BF16 pairs, written over the first 64 score columns
+            // in two stores: the first is in flight while the second half is
+            // computed
+            uint32_t pa[32], pb[32];
             float2 ps[4] = {};
             const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-base, -base);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {  // paired FP32 arithmetic: two columns per instruction
+            for (int c = 0; c < 32; ++c) {  // paired FP32 arithmetic: two columns per instruction
                 const float2 e = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
                 const float p0 = ex2(e.x), p1 = ex2(e.y);
                 ps[c & 3] = __fadd2_rn(ps[c & 3], make_float2(p0, p1));
-                pk[c] = __uint_as_float(pack_bf16x2(p0, p1));
+                pa[c] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32_nowait(scol, pa);
+#pragma unroll
+            for (int c = 32; c < 64; ++c) {
+                const float2 e = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
+                const float p0 = ex2(e.x), p1 = ex2(e.y);
+                ps[c & 3] = __fadd2_rn(ps[c & 3], make_float2(p0, p1));
+                pb[c - 32] = pack_bf16x2(p0, p1);
             }
             const float2 pq = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
             l = l * factor + (pq.x + pq.y);
@@ -396,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32x2(ocol + 64 * hf, ocol + 64 * hf + 32, o);
                 }
             }
-            tmem_st32x2(scol, scol + 32, pk);  // P over the first 64 score columns
+            tmem_st32_nowait(scol + 32, pb);
+            tmem_wait_st32x2(pa, pb);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x]);
