@@ -7,8 +7,9 @@ with a ragged last block, prefills (L = q_len) at every tile-boundary length,
 extends over short and long cached prefixes, rows that see no token (L <
 q_len), groups G = 1 .. 16, NaN-poisoned free slots in the last pages.  The
 Table-4 shapes of the vLLM post are compared on sampled rows that include the
-first and last query tokens and the 128-token block edges.  Plus run-to-run
-determinism and the kernel's own flags for bad lengths and pages."""
+first and last query tokens and the 128-token block edges.  Plus seeded
+random batches, run-to-run determinism, page-permutation invariance and the
+kernel's own flags for bad lengths and pages."""
 
 import numpy as np
 import pytest
@@ -159,3 +160,19 @@ def test_unsupported_shapes_are_refused():
     with pytest.raises(hd.HpcError):
         hd.hpc_prefill_attn(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
                             batch.seqlens, 6, 4, 100, 0.088, out)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(seed):
+    """Seeded random batches: 1-4 requests, q_len 1..300, lengths below and
+    above q_len (up to 3000 tokens of prefix), G in {1, 2, 4, 8}."""
+    rng = np.random.default_rng(900 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    q_len = int(rng.integers(1, 301))
+    B = int(rng.integers(1, 5))
+    lens = [int(q_len + rng.integers(-min(q_len, 40), 3000)) for _ in range(B)]
+    lens = [max(L, 0) for L in lens]
+    batch = small(f"rand{seed}", lens, g * hkv, hkv, q_len, 950 + seed)
+    got = run_prefill(batch)
+    assert_close(got.reshape(-1, 128), oracle_rows(batch).reshape(-1, 128), "bf16")
