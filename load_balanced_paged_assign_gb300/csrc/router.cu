@@ -16,8 +16,11 @@
 //     into the W_low accumulator, both in TMEM (hi at column 0, lo after it);
 //     tcgen05.commit releases each stage when its MMAs are done;
 //   * warps 2-5 wait for the last commit, read both accumulators with
-//     tcgen05.ld (warp w reads TMEM lanes 32 (w mod 4) ..), and write
-//     hi + lo / 256 (exact scaling) as FP32 scores, or as a split's partial;
+//     tcgen05.ld (warp w reads TMEM lanes 32 (w mod 4) ..), form
+//     hi + lo / 256 (exact scaling), stage it in the freed ring (32-column
+//     chunks, 128-byte swizzle) and write each chunk with a TMA tensor store,
+//     as FP32 scores or as a split's partial (rows past M and columns past N
+//     fall outside the tensor map and are not written);
 //   * with split-K a second kernel sums the partials in a fixed order, so the
 //     result is deterministic;
 //   * up to 16 tokens the product is a weight-bound matrix-vector product:
@@ -42,17 +45,17 @@ constexpr int kUK = 16;         // K per MMA instruction (kind::f16)
 constexpr int kMaxBN = 256;     // experts per CTA (UMMA N limit at M = 128)
 constexpr int kThreads = 192;   // producer, MMA, 4 epilogue warps
 constexpr int kMaxStages = 4;
+constexpr int kRingBytes = 200 * 1024;  // shared memory given to the stages at most
 constexpr int kSmemFloor = 120 * 1024;  // keeps one CTA per SM: TMEM is never contended
 
 struct RouterArgs {
-    float *out;       // [M, N] scores (splits == 1)
-    float *partials;  // [splits, M, N] (splits > 1)
     int32_t *flags;   // optional error word
     int M, N, K;
-    int bn;           // experts per CTA (multiple of 16, <= 256)
-    int kb_per_split; // K blocks of 64 per split
+    int bn;           // experts per CTA (multiple of 32, <= 256)
+    int kb_per_split; // K blocks per split
     int splits;
     int stages;
+    int bar_off;      // shared-memory offset of the barriers (after the ring and the staging tile)
     int lo_col;       // TMEM column of the W_low accumulator
     uint32_t tmem_cols;
 };
@@ -62,12 +65,13 @@ __host__ __device__ inline int stage_bytes(int bn) { return kBM * kBK * 2 + 2 * 
 __global__ void __launch_bounds__(kThreads, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tx,
                        const __grid_constant__ CUtensorMap thi,
-                       const __grid_constant__ CUtensorMap tlo, const RouterArgs a) {
+                       const __grid_constant__ CUtensorMap tlo,
+                       const __grid_constant__ CUtensorMap tout, const RouterArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int sb = stage_bytes(a.bn);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.stages * sb);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.bar_off);
     uint64_t *empty = full + kMaxStages;
     uint64_t *tmem_full = empty + kMaxStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmem_full + 1);
@@ -145,31 +149,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(tmem_full);
         }
     } else {
-        // epilogue: TMEM lane quarter q = warp mod 4 holds rows 32 q .. 32 q + 31
+        // epilogue: TMEM lane quarter q = warp mod 4 holds rows 32 q .. 32 q + 31.
+        // The ring is free once the last commit has arrived; each warp stages
+        // its 32 rows there as 32-column chunks (128-byte rows, 128-byte
+        // swizzle: a warp's 16-byte writes fill whole bank rows) and stores
+        // each chunk with one TMA tensor store.  Rows past M and columns past
+        // N fall outside the tensor map and are not written.
         const int q = warp & 3;
+        // (after an abort, copies may still land in the ring: nothing is staged)
         int live = 1;
-        if (lane == 0) live = mbar_wait(tmem_full, 0, abort) ? 1 : 0;
+        if (lane == 0) live = mbar_wait(tmem_full, 0, abort) && !*abort ? 1 : 0;
         live = __shfl_sync(0xffffffffu, live, 0);
         if (live) {
             mbar_try_wait(tmem_full, 0);  // every lane observes the completed phase
             tc_fence_after();
-            const int m = m0 + 32 * q + lane;
             const uint32_t row = tmem + ((uint32_t)(32 * q) << 16);
-            float *dst = a.splits == 1 ? a.out + (size_t)m * a.N
-                                       : a.partials + ((size_t)split * a.M + m) * a.N;
-            for (int c = 0; c < a.bn; c += 16) {
-                float hi[16], lo[16];
-                tmem_ld16x2(row + c, row + a.lo_col + c, hi, lo);
-                if (m < a.M && n0 + c < a.N && !*abort) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + n0 + c);
+            const int chunks = a.bn / 32;
+            uint8_t *stage_out = smem + (size_t)q * chunks * 4096;
+            for (int c = 0; c < chunks; ++c) {
+                float v[64];
+                tmem_ld32x2(row + 32 * c, row + a.lo_col + 32 * c, v);
+                uint8_t *line = stage_out + c * 4096 + lane * 128;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        d4[j] = make_float4(hi[4 * j] + lo[4 * j] * (1.0f / 256.0f),
-                                            hi[4 * j + 1] + lo[4 * j + 1] * (1.0f / 256.0f),
-                                            hi[4 * j + 2] + lo[4 * j + 2] * (1.0f / 256.0f),
-                                            hi[4 * j + 3] + lo[4 * j + 3] * (1.0f / 256.0f));
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(line + ((j ^ (lane & 7)) << 4)) =
+                        make_float4(v[4 * j] + v[32 + 4 * j] * (1.0f / 256.0f),
+                                    v[4 * j + 1] + v[32 + 4 * j + 1] * (1.0f / 256.0f),
+                                    v[4 * j + 2] + v[32 + 4 * j + 2] * (1.0f / 256.0f),
+                                    v[4 * j + 3] + v[32 + 4 * j + 3] * (1.0f / 256.0f));
+                fence_proxy_async_smem();  // the writes are seen by the TMA store
+                __syncwarp();
+                if (lane == 0 && !*abort) {
+                    tma_store_3d(&tout, stage_out + c * 4096, n0 + 32 * c, m0 + 32 * q, split);
+                    bulk_commit_group();
                 }
             }
+            if (lane == 0) bulk_wait_all();  // the scores are written, the staging is free
+            __syncwarp();
         } else {
             ok = false;
         }
@@ -416,13 +432,26 @@ int sm_count(int dev) {
 }
 
 struct Plan {
-    int bn, n_tiles, m_tiles, splits, kb_per_split, stages, smem;
+    int bn, n_tiles, m_tiles, splits, kb_per_split, stages, bar_off, smem;
 };
+
+// Ring depth and shared-memory layout for the plan's tile: the stages, then
+// (overlapping them) the epilogue's staging tile of 128 x bn FP32 scores,
+// then the barriers.
+void size_ring(Plan &p) {
+    const int sb = stage_bytes(p.bn);
+    p.stages = std::min(kMaxStages, std::max(2, kRingBytes / sb));
+    p.stages = std::max(1, std::min(p.stages, p.kb_per_split));
+    p.bar_off = std::max(p.stages * sb, kBM * p.bn * 4);
+    p.smem = std::max(kSmemFloor, p.bar_off + 2 * kMaxStages * 8 + 8 + 16 + 1024);
+}
 
 Plan plan_for(int M, int N, int K, int sms) {
     Plan p;
     p.n_tiles = (N + kMaxBN - 1) / kMaxBN;
-    p.bn = ((N / p.n_tiles + 15) / 16) * 16;
+    // experts per CTA: a multiple of 32 (whole 32-column store chunks); the
+    // last tile's rows past N read as zeros and its columns past N are not stored
+    p.bn = (((N + p.n_tiles - 1) / p.n_tiles + 31) / 32) * 32;
     p.m_tiles = (M + kBM - 1) / kBM;
     const int kbs = K / kBK;
     // split K when the tiles alone would leave SMs idle; every split keeps
@@ -432,11 +461,7 @@ Plan plan_for(int M, int N, int K, int sms) {
     while (kbs % want) --want;
     p.splits = want;
     p.kb_per_split = kbs / want;
-    const int sb = stage_bytes(p.bn);
-    p.stages = std::min(kMaxStages, std::max(2, (200 * 1024) / sb));
-    p.stages = std::min(p.stages, std::max(1, p.kb_per_split));
-    p.stages = std::max(p.stages, 1);
-    p.smem = std::max(kSmemFloor, p.stages * sb + 2 * kMaxStages * 8 + 8 + 16 + 1024);
+    size_ring(p);
     return p;
 }
 
@@ -493,7 +518,7 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
             while (kbs % fit) --fit;
             p.splits = fit;
             p.kb_per_split = kbs / fit;
-            p.stages = std::min(kMaxStages, std::max(2, (200 * 1024) / stage_bytes(p.bn)));
+            size_ring(p);
         }
     }
     auto encode = tensor_map_encoder();
@@ -522,9 +547,22 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return HPC_ERR_CUDA;
     }
+    // scores (one split) or the splits' partials, [splits, M, N] FP32, stored
+    // in 32 x 32 tiles with the 128-byte swizzle of the staging chunks
+    CUtensorMap tout;
+    {
+        void *base = p.splits > 1 ? d_workspace : static_cast<void *>(d_out);
+        const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)p.splits};
+        const cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)M * N * 4};
+        const cuuint32_t box[3] = {32, 32, 1};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (encode(&tout, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return HPC_ERR_CUDA;
+    }
     RouterArgs a;
-    a.out = d_out;
-    a.partials = static_cast<float *>(d_workspace);
     a.flags = d_flags;
     a.M = M;
     a.N = N;
@@ -533,11 +571,10 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
     a.kb_per_split = p.kb_per_split;
     a.splits = p.splits;
     a.stages = p.stages;
-    a.lo_col = ((p.bn + 31) / 32) * 32;
+    a.bar_off = p.bar_off;
+    a.lo_col = p.bn;  // a multiple of 32
     a.tmem_cols = 32;
     while (a.tmem_cols < (uint32_t)(a.lo_col + p.bn)) a.tmem_cols <<= 1;
-    p.smem = std::max(kSmemFloor, a.stages * stage_bytes(p.bn) + 2 * kMaxStages * 8 + 8 + 16 +
-                                      1024);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (p.smem > g_smem_set[dev]) {
@@ -559,7 +596,7 @@ extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, router_gemm_kernel, tx, thi, tlo, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, router_gemm_kernel, tx, thi, tlo, tout, a);
     if (e == cudaSuccess && p.splits > 1) {
         const size_t n4 = (size_t)M * N / 4;
         const bool few = p.splits <= 8;

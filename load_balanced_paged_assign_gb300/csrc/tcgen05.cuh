@@ -56,6 +56,27 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
            ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// 3-D tiled TMA store from shared memory, tracked by the thread's bulk
+// groups; elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+            "l"(map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk group this thread committed has completed (its
+// global writes done, its shared-memory source free).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of an MN-major operand stored with the
 // 128-byte swizzle: each K index is a row of 128 bytes holding 64 consecutive
 // MN elements, 8-row groups 1024 bytes apart (stride offset), and the next

@@ -65,7 +65,8 @@ def test_scores_against_the_oracle(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (200, 272, 128), (129, 256, 4096),
-                                   (3, 192, 4096), (700, 64, 1024)])
+                                   (3, 192, 4096), (700, 64, 1024), (77, 176, 512),
+                                   (1000, 48, 256), (4100, 192, 4096), (40, 16, 128)])
 def test_other_shapes(M, N, K):
     x, w = make_router_inputs(M, K=K, N=N, seed=1500 + M + N, device="cuda")
     hi, lo = split_gpu(w)
@@ -74,11 +75,29 @@ def test_other_shapes(M, N, K):
     assert np.abs(got - ref).max() <= ACC_TOL * max(1.0, (K / 4096) ** 0.5)
 
 
-def test_split_k_matches_a_single_pass_and_is_deterministic():
-    x, w = make_router_inputs(16, seed=1601, device="cuda")
+@pytest.mark.parametrize("M", [16, 64, 300, 4096])
+def test_split_k_matches_a_single_pass_and_is_deterministic(M):
+    x, w = make_router_inputs(M, seed=1601 + M, device="cuda")
     hi, lo = split_gpu(w)
     a = gemm_gpu(x, hi, lo, use_workspace=True)
     b = gemm_gpu(x, hi, lo, use_workspace=True)
     c = gemm_gpu(x, hi, lo, use_workspace=False)  # no room for partials: one pass
     assert torch.equal(a, b)
     assert (a - c).abs().max().item() <= ACC_TOL
+
+
+@pytest.mark.parametrize("M,N", [(300, 192), (129, 176), (5000, 48)])
+def test_nothing_is_written_past_the_scores(M, N):
+    """The scores are a view into a larger buffer: the rows after them keep
+    their sentinel (the tail tile's rows past M are clipped by the store)."""
+    x, w = make_router_inputs(M, K=1024, N=N, seed=1700 + M, device="cuda")
+    hi, lo = split_gpu(w)
+    buf = torch.full((M + 130, N), 7.0, device="cuda")
+    out = buf[:M]
+    nbytes = hd.hpc_router_workspace_bytes(M, N, 1024)
+    ws = torch.empty(max(nbytes // 4, 1), device="cuda") if nbytes > 0 else None
+    hd.hpc_router_gemm(x, hi, lo, out, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(buf[M:], torch.full_like(buf[M:], 7.0))
+    ref = ro.router_scores(bits16(x), bits16(hi), bits16(lo))
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= ACC_TOL
