@@ -524,6 +524,16 @@ hpc_status hpc_router_split(const float *d_w, int32_t N, int32_t K, void *d_w_hi
 int64_t hpc_router_workspace_bytes(int32_t M, int32_t N, int32_t K);
 
 /*
+ * The launch hpc_router_gemm makes for this shape on the current device with
+ * a full workspace, in plan[4] (host int32): plan[0] = 1 for the tensor-core
+ * kernel, 0 for the few-token CUDA-core kernel (M <= 16); plan[1] = experts
+ * per CTA; plan[2] = K splits; plan[3] = CTAs launched.  HPC_ERR_ARG /
+ * HPC_ERR_UNSUPPORTED as hpc_router_gemm; HPC_ERR_CUDA when the tensor-core
+ * plan needs a device and none is present.
+ */
+hpc_status hpc_router_plan(int32_t M, int32_t N, int32_t K, int32_t *plan);
+
+/*
  * S = X W_high^T + (X W_low^T) / 256 for d_x (device bf16 [M, K], row-major
  * tokens x hidden) into d_out (device fp32 [M, N]).  K must be a multiple of
  * 64 and N of 16 (HPC_ERR_UNSUPPORTED otherwise); all pointers 16-byte

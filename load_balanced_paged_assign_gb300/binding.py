@@ -28,7 +28,7 @@ EXPORTS = (
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
     "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
     "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
-    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_gemm", "hpc_prefill_attn",
+    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_plan", "hpc_router_gemm", "hpc_prefill_attn",
     "hpc_decode_packed_layout", "hpc_decode_step_host_packed",
 )
 
@@ -105,6 +105,7 @@ def lib():
         "hpc_rope_frequencies": (ctypes.c_int, [f32, vp, vp]),
         "hpc_router_split": (ctypes.c_int, [vp, i32, i32, vp, vp, vp]),
         "hpc_router_workspace_bytes": (i64, [i32, i32, i32]),
+        "hpc_router_plan": (ctypes.c_int, [i32, i32, i32, vp]),
         "hpc_router_gemm": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
         "hpc_prefill_attn": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                             i32, f32, vp, vp, vp]),
@@ -334,6 +335,14 @@ def hpc_router_split(w, w_hi, w_lo, stream=None):
 
 def hpc_router_workspace_bytes(M, N, K) -> int:
     return int(lib().hpc_router_workspace_bytes(int(M), int(N), int(K)))
+
+
+def hpc_router_plan(M, N, K) -> dict:
+    """The launch hpc_router_gemm makes for this shape on the current device."""
+    plan = (ctypes.c_int32 * 4)()
+    _check("hpc_router_plan", lib().hpc_router_plan(int(M), int(N), int(K), plan))
+    return {"tensor_cores": bool(plan[0]), "bn": int(plan[1]), "splits": int(plan[2]),
+            "ctas": int(plan[3])}
 
 
 def hpc_router_gemm(x, w_hi, w_lo, out, workspace=None, flags=None, stream=None):

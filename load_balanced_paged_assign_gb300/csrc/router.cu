@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();  // X may come from the kernel before this one
+    // with split-K the reduction kernel follows: let it be scheduled now (it
+    // waits for this grid's completion before reading the partials), so its
+    // launch latency overlaps this kernel
+    if (a.splits > 1) grid_launch_dependents();
 
     bool ok = true;
     int issued = 0;  // (producer lane) stages whose copies were issued
@@ -488,6 +492,25 @@ extern "C" int64_t hpc_router_workspace_bytes(int32_t M, int32_t N, int32_t K) {
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     const Plan p = plan_for(M, N, K, sm_count(dev));
     return p.splits > 1 ? (int64_t)p.splits * M * N * 4 : 0;
+}
+
+extern "C" hpc_status hpc_router_plan(int32_t M, int32_t N, int32_t K, int32_t *plan) {
+    if (!plan || M < 0 || N <= 0 || K <= 0) return HPC_ERR_ARG;
+    if (K % kBK || N % 16) return HPC_ERR_UNSUPPORTED;
+    plan[0] = plan[1] = plan[2] = plan[3] = 0;
+    if (M == 0) return HPC_OK;
+    if (M <= kGemvMaxM) {
+        plan[3] = (N + kGemvExperts - 1) / kGemvExperts;
+        return HPC_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HPC_ERR_CUDA;
+    const Plan p = plan_for(M, N, K, sm_count(dev));
+    plan[0] = 1;
+    plan[1] = p.bn;
+    plan[2] = p.splits;
+    plan[3] = p.m_tiles * p.n_tiles * p.splits;
+    return HPC_OK;
 }
 
 extern "C" hpc_status hpc_router_gemm(const void *d_x, const void *d_w_hi, const void *d_w_lo,

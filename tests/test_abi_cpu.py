@@ -226,6 +226,13 @@ def test_router_argument_checks(hd):
     assert L.hpc_router_split(FAKE, 0, 4096, FAKE, FAKE, None) == E.HPC_ERR_ARG
     assert L.hpc_router_workspace_bytes(4, 192, 4000) == -1
     assert L.hpc_router_workspace_bytes(0, 192, 4096) == 0
+    plan = (ctypes.c_int32 * 4)()
+    assert L.hpc_router_plan(4, 192, 4000, plan) == E.HPC_ERR_UNSUPPORTED
+    assert L.hpc_router_plan(4, 192, 4096, None) == E.HPC_ERR_ARG
+    assert L.hpc_router_plan(-1, 192, 4096, plan) == E.HPC_ERR_ARG
+    assert L.hpc_router_plan(0, 192, 4096, plan) == E.HPC_OK and list(plan) == [0, 0, 0, 0]
+    # few tokens: the CUDA-core kernel, two experts per CTA (no device needed)
+    assert L.hpc_router_plan(16, 192, 4096, plan) == E.HPC_OK and list(plan) == [0, 0, 0, 96]
 
 
 def test_prefill_argument_checks(hd):

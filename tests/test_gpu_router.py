@@ -50,7 +50,7 @@ def test_split_matches_the_oracle_bit_for_bit():
     assert np.array_equal(bits16(hi), ref_hi) and np.array_equal(bits16(lo), ref_lo)
 
 
-@pytest.mark.parametrize("M", [1, 5, 64, 127, 128, 129, 300, 1024, 4096])
+@pytest.mark.parametrize("M", [1, 5, 17, 64, 127, 128, 129, 300, 1024, 4096, 16384])
 def test_scores_against_the_oracle(M):
     x, w = make_router_inputs(M, seed=1400 + M, device="cuda")
     hi, lo = split_gpu(w)
@@ -66,7 +66,8 @@ def test_scores_against_the_oracle(M):
 
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (200, 272, 128), (129, 256, 4096),
                                    (3, 192, 4096), (700, 64, 1024), (77, 176, 512),
-                                   (1000, 48, 256), (4100, 192, 4096), (40, 16, 128)])
+                                   (1000, 48, 256), (4100, 192, 4096), (40, 16, 128),
+                                   (5000, 48, 1024), (2000, 512, 512)])
 def test_other_shapes(M, N, K):
     x, w = make_router_inputs(M, K=K, N=N, seed=1500 + M + N, device="cuda")
     hi, lo = split_gpu(w)
@@ -84,6 +85,20 @@ def test_split_k_matches_a_single_pass_and_is_deterministic(M):
     c = gemm_gpu(x, hi, lo, use_workspace=False)  # no room for partials: one pass
     assert torch.equal(a, b)
     assert (a - c).abs().max().item() <= ACC_TOL
+
+
+def test_plans_reported_for_the_sweep():
+    """The plan query reports the launch: the CUDA-core kernel up to 16
+    tokens, K split over more CTAs the fewer the tokens, no split once the
+    token tiles alone fill the GPU."""
+    few = hd.hpc_router_plan(16, 192, 4096)
+    assert not few["tensor_cores"] and few["ctas"] == 96
+    plans = [hd.hpc_router_plan(M, 192, 4096) for M in (64, 1024, 4096, 16384)]
+    assert all(p["tensor_cores"] and p["bn"] == 192 for p in plans)
+    splits = [p["splits"] for p in plans]
+    assert splits == sorted(splits, reverse=True) and splits[0] > 1 and splits[-1] == 1
+    assert all(p["ctas"] <= torch.cuda.get_device_properties(0).multi_processor_count
+               for p in plans)
 
 
 @pytest.mark.parametrize("M,N", [(300, 192), (129, 176), (5000, 48)])
