@@ -148,16 +148,88 @@ __device__ __forceinline__ void store_bf16(char *row, int s, const float (&y)[8]
                                    pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7])));
 }
 
-// cs = (cos, sin) of this sub-lane's four frequencies, interleaved.
+// The rotation of this sub-lane's four pairs: c, sn = cos, sin of its four
+// frequencies, nsn = -sin.  In the halves layout pairs k and k + 1 sit in
+// consecutive registers, so two pairs take one paired FP32 instruction
+// (each lane of which rounds like the scalar one).
 template <int LAYOUT>
-__device__ __forceinline__ void rotate(float (&x)[8], const float (&cs)[8]) {
+__device__ __forceinline__ void rotate(float (&x)[8], const float (&c)[4], const float (&sn)[4],
+                                       const float (&nsn)[4]) {
+    if constexpr (LAYOUT == HPC_ROPE_HALVES) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int ia = LAYOUT == HPC_ROPE_HALVES ? k : 2 * k;
-        const int ib = LAYOUT == HPC_ROPE_HALVES ? 4 + k : 2 * k + 1;
-        const float p = x[ia], q = x[ib], c = cs[2 * k], sn = cs[2 * k + 1];
-        x[ia] = fmaf(p, c, -q * sn);
-        x[ib] = fmaf(q, c, p * sn);
+        for (int h = 0; h < 2; ++h) {
+            const float2 p = make_float2(x[2 * h], x[2 * h + 1]);
+            const float2 q = make_float2(x[4 + 2 * h], x[5 + 2 * h]);
+            const float2 cc = make_float2(c[2 * h], c[2 * h + 1]);
+            const float2 p2 = __ffma2_rn(p, cc, __fmul2_rn(q, make_float2(nsn[2 * h], nsn[2 * h + 1])));
+            const float2 q2 = __ffma2_rn(q, cc, __fmul2_rn(p, make_float2(sn[2 * h], sn[2 * h + 1])));
+            x[2 * h] = p2.x, x[2 * h + 1] = p2.y;
+            x[4 + 2 * h] = q2.x, x[5 + 2 * h] = q2.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float p = x[2 * k], q = x[2 * k + 1];
+            x[2 * k] = fmaf(p, c[k], q * nsn[k]);
+            x[2 * k + 1] = fmaf(q, c[k], p * sn[k]);
+        }
+    }
+}
+
+// x[k] *= m[k] for the 8 values, two per instruction.
+__device__ __forceinline__ void mul8(float (&x)[8], const float (&m)[8]) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 v = __fmul2_rn(make_float2(x[2 * h], x[2 * h + 1]),
+                                    make_float2(m[2 * h], m[2 * h + 1]));
+        x[2 * h] = v.x, x[2 * h + 1] = v.y;
+    }
+}
+
+// x[k] *= m for the 8 values, two per instruction.
+__device__ __forceinline__ void scale8(float (&x)[8], float m) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 v = __fmul2_rn(make_float2(x[2 * h], x[2 * h + 1]), make_float2(m, m));
+        x[2 * h] = v.x, x[2 * h + 1] = v.y;
+    }
+}
+
+// Sum of squares of the 8 values (two partial sums, paired).
+__device__ __forceinline__ float sumsq8(const float (&x)[8]) {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 v = make_float2(x[2 * h], x[2 * h + 1]);
+        acc = __ffma2_rn(v, v, acc);
+    }
+    return acc.x + acc.y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float absmax8(const float (&x)[8]) {
+    return fmax3(fmax3(fabsf(x[0]), fabsf(x[1]), fabsf(x[2])),
+                 fmax3(fabsf(x[3]), fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7])));
+}
+
+// x[k] / s correctly rounded to FP32 for the 8 values, from y = RN(1/s):
+// q = RN(x y) is within an ulp of x / s, r = x - s q is exact (one FMA), and
+// RN(q + r y) is the correctly rounded quotient (Markstein's theorem on
+// division with a fused multiply-add); two values per instruction.
+__device__ __forceinline__ void div8(float (&x)[8], float s, float y) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 v = make_float2(x[2 * h], x[2 * h + 1]);
+        const float2 q = __fmul2_rn(v, make_float2(y, y));
+        const float2 r = __ffma2_rn(make_float2(-s, -s), q, v);
+        const float2 o = __ffma2_rn(r, make_float2(y, y), q);
+        x[2 * h] = o.x, x[2 * h + 1] = o.y;
     }
 }
 
@@ -169,7 +241,8 @@ __device__ __forceinline__ void rotate(float (&x)[8], const float (&cs)[8]) {
 template <bool FP8, int LAYOUT, bool NF, int KIND, int NP>
 __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *stage, int t,
                                            int row0, int end, int half, int s,
-                                           const float (&cs)[8], long long slot,
+                                           const float (&c)[4], const float (&sn)[4],
+                                           const float (&nsn)[4], long long slot,
                                            const float (&w)[8], float kv_scale) {
     constexpr int kElem = FP8 ? 1 : 2;
     if (KIND != kQ && slot < 0) return;  // no cache slot for this token (uniform per CTA)
@@ -196,13 +269,13 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
 #pragma unroll
         for (int i = 0; i < NP; ++i)
             unpack8(load_words<LAYOUT>(stage + (size_t)row[i] * kRowBytes, s), x[i]);
-        if constexpr (KIND == kV) {  // FP8 value rows: true division by the cache scale
-            // (BF16 inputs over the scale often land exactly on an E4M3
-            // midpoint, where only the exact quotient rounds to even)
+        if constexpr (KIND == kV) {  // FP8 value rows: the correctly rounded quotient by
+            // the cache scale (BF16 inputs over the scale often land exactly
+            // on an E4M3 midpoint, where only the exact quotient rounds to even)
+            const float y = __frcp_rn(kv_scale);
 #pragma unroll
             for (int i = 0; i < NP; ++i) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) x[i][k] = __fdiv_rn(x[i][k], kv_scale);
+                div8(x[i], kv_scale, y);
                 if (valid[i])
                     store_e4m3<LAYOUT>(static_cast<char *>(a.v_cache) +
                                            (slot * a.Hkv + (row[i] - a.Hq - a.Hkv)) * kHeadDim,
@@ -214,12 +287,7 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
             // weighted row before the norm factor: the output is inv * v
             float inv[NP];
 #pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                float ss = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) ss = fmaf(x[i][k], x[i][k], ss);
-                inv[i] = ss;
-            }
+            for (int i = 0; i < NP; ++i) inv[i] = sumsq8(x[i]);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
 #pragma unroll
@@ -228,13 +296,11 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
             for (int i = 0; i < NP; ++i) {
                 inv[i] = rsqrtf(fmaf(inv[i], 1.0f / kHeadDim, a.eps));
                 if constexpr (NF) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[i][k] *= w[k];
-                    rotate<LAYOUT>(x[i], cs);
+                    mul8(x[i], w);
+                    rotate<LAYOUT>(x[i], c, sn, nsn);
                 } else {
-                    rotate<LAYOUT>(x[i], cs);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[i][k] *= w[k];
+                    rotate<LAYOUT>(x[i], c, sn, nsn);
+                    mul8(x[i], w);
                 }
             }
             if constexpr (KIND == kQ) {
@@ -243,12 +309,7 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
                     // scale is amax(inv * v) / 448
                     float amax[NP];
 #pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        float m = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(x[i][k]));
-                        amax[i] = m;
-                    }
+                    for (int i = 0; i < NP; ++i) amax[i] = absmax8(x[i]);
 #pragma unroll
                     for (int o = 8; o > 0; o >>= 1)
 #pragma unroll
@@ -259,8 +320,7 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
                         const float ymax = amax[i] * inv[i];
                         const bool live = ymax > 0.f;
                         const float mul = live ? __fdividef(448.0f, amax[i]) : 0.f;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) x[i][k] *= mul;
+                        scale8(x[i], mul);
                         if (valid[i]) {
                             const size_t qrow = (size_t)t * a.Hq + row[i];
                             store_e4m3<LAYOUT>(static_cast<char *>(a.q_out) + qrow * kHeadDim, s,
@@ -271,8 +331,7 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
                 } else {
 #pragma unroll
                     for (int i = 0; i < NP; ++i) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) x[i][k] *= inv[i];
+                        scale8(x[i], inv[i]);
                         if (valid[i])
                             store_bf16<LAYOUT>(static_cast<char *>(a.q_out) +
                                                    ((size_t)t * a.Hq + row[i]) * (kHeadDim * 2),
@@ -283,8 +342,7 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
 #pragma unroll
                 for (int i = 0; i < NP; ++i) {
                     const float m = FP8 ? inv[i] * __frcp_rn(kv_scale) : inv[i];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[i][k] *= m;
+                    scale8(x[i], m);
                     if (!valid[i]) continue;
                     char *dst = static_cast<char *>(a.k_cache) +
                                 (slot * a.Hkv + (row[i] - a.Hq)) * (kHeadDim * kElem);
@@ -302,16 +360,17 @@ __device__ __forceinline__ void rows_batch(const RopeNormArgs &a, const char *st
 template <bool FP8, int LAYOUT, bool NF, int KIND>
 __device__ __forceinline__ void rows_of_kind(const RopeNormArgs &a, const char *stage, int t,
                                              int begin, int end, int pair0, int warp, int half,
-                                             int s, const float (&cs)[8], long long slot,
+                                             int s, const float (&c)[4], const float (&sn)[4],
+                                             const float (&nsn)[4], long long slot,
                                              const float (&w)[8], float kv_scale) {
     const int npairs = (end - begin + 1) / 2;
     int p = ((warp - pair0) % kRnWarps + kRnWarps) % kRnWarps;  // first pair of this warp
     int count = p < npairs ? (npairs - 1 - p) / kRnWarps + 1 : 0;
     for (; count >= 2; count -= 2, p += 2 * kRnWarps)
-        rows_batch<FP8, LAYOUT, NF, KIND, 2>(a, stage, t, begin + 2 * p, end, half, s, cs, slot, w,
-                                         kv_scale);
-    if (count) rows_batch<FP8, LAYOUT, NF, KIND, 1>(a, stage, t, begin + 2 * p, end, half, s, cs,
-                                                slot, w, kv_scale);
+        rows_batch<FP8, LAYOUT, NF, KIND, 2>(a, stage, t, begin + 2 * p, end, half, s, c, sn, nsn,
+                                             slot, w, kv_scale);
+    if (count) rows_batch<FP8, LAYOUT, NF, KIND, 1>(a, stage, t, begin + 2 * p, end, half, s, c,
+                                                    sn, nsn, slot, w, kv_scale);
 }
 
 // cos/sin of pos * freq_i, freq_i = hi + lo (two floats), reduced modulo 2 pi.
@@ -329,6 +388,12 @@ __device__ __forceinline__ float2 rope_angle(int pos, float hi, float lo) {
     float s, c;
     sincospif(r * kInvPi, &s, &c);
     return make_float2(c, s);
+}
+
+// (cos, sin) of frequency i into a buffer of the angle table.
+__device__ __forceinline__ void store_angle(float *tab, int i, float2 cs) {
+    tab[(i >> 2) * 8 + (i & 3)] = cs.x;
+    tab[(i >> 2) * 8 + 4 + (i & 3)] = cs.y;
 }
 
 // The token's cache slot (page * 64 + offset), or -1 with a flag raised.
@@ -361,8 +426,10 @@ __global__ void __launch_bounds__(kRnThreads, HPC_RN_MIN_CTAS) rope_norm_kernel(
     extern __shared__ __align__(128) unsigned char smem[];
     const int row_bytes = a.R * kRowBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * row_bytes);
-    float2 *s_cs = reinterpret_cast<float2 *>(full + kMaxStages);  // [2][64]
-    float *s_fhi = reinterpret_cast<float *>(s_cs + 2 * 64);
+    // [2][128]: per buffer and group g of frequencies 4g .. 4g + 3, their
+    // four cosines then their four sines
+    float *s_ang = reinterpret_cast<float *>(full + kMaxStages);
+    float *s_fhi = s_ang + 2 * 128;
     float *s_flo = s_fhi + 64;
     long long *s_slot = reinterpret_cast<long long *>(s_flo + 64);  // [2]
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_slot + 2);
@@ -408,7 +475,7 @@ __global__ void __launch_bounds__(kRnThreads, HPC_RN_MIN_CTAS) rope_norm_kernel(
     __syncthreads();  // barriers initialised, frequency table ready
 
     // angles and cache slot of the first token
-    if (tid < 64) s_cs[tid] = rope_angle(pos0, s_fhi[tid], s_flo[tid]);
+    if (tid < 64) store_angle(s_ang, tid, rope_angle(pos0, s_fhi[tid], s_flo[tid]));
     else if (tid == 64) s_slot[0] = token_slot(a, blockIdx.x, pos0, req0);
 
     bool ok = true;
@@ -429,24 +496,26 @@ __global__ void __launch_bounds__(kRnThreads, HPC_RN_MIN_CTAS) rope_norm_kernel(
         if (ok) ok = warp_wait_phase(&full[stage], (uint32_t)(it / a.stages) & 1u, s_abort);
         if (ok) {
             const char *st = reinterpret_cast<const char *>(smem) + (size_t)stage * row_bytes;
-            float cs[8];
+            float c[4], sn[4], nsn[4];
             {
-                const float4 *c4 = reinterpret_cast<const float4 *>(s_cs + buf * 64 + 4 * sub);
-                const float4 c0 = c4[0], c1 = c4[1];
-                cs[0] = c0.x, cs[1] = c0.y, cs[2] = c0.z, cs[3] = c0.w;
-                cs[4] = c1.x, cs[5] = c1.y, cs[6] = c1.z, cs[7] = c1.w;
+                const float4 *a4 = reinterpret_cast<const float4 *>(s_ang + buf * 128 + 8 * sub);
+                const float4 c4 = a4[0], s4 = a4[1];
+                c[0] = c4.x, c[1] = c4.y, c[2] = c4.z, c[3] = c4.w;
+                sn[0] = s4.x, sn[1] = s4.y, sn[2] = s4.z, sn[3] = s4.w;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) nsn[k] = -sn[k];
             }
             const long long slot = s_slot[buf];
             const int pq = (a.Hq + 1) / 2, pk = (a.Hkv + 1) / 2;  // pairs of each kind
-            rows_of_kind<FP8, LAYOUT, NF, kQ>(a, st, t, 0, a.Hq, 0, warp, half, sub, cs, slot, wq,
+            rows_of_kind<FP8, LAYOUT, NF, kQ>(a, st, t, 0, a.Hq, 0, warp, half, sub, c, sn, nsn, slot, wq,
                                           1.f);
-            rows_of_kind<FP8, LAYOUT, NF, kK>(a, st, t, a.Hq, a.Hq + a.Hkv, pq, warp, half, sub, cs,
+            rows_of_kind<FP8, LAYOUT, NF, kK>(a, st, t, a.Hq, a.Hq + a.Hkv, pq, warp, half, sub, c, sn, nsn,
                                           slot, wk, a.k_scale);
             rows_of_kind<FP8, LAYOUT, NF, kV>(a, st, t, a.Hq + a.Hkv, a.R, pq + pk, warp, half, sub,
-                                          cs, slot, wk, a.v_scale);
+                                          c, sn, nsn, slot, wk, a.v_scale);
         }
         if (has_next) {
-            if (tid < 64) s_cs[(buf ^ 1) * 64 + tid] = rope_angle(pos_n, s_fhi[tid], s_flo[tid]);
+            if (tid < 64) store_angle(s_ang + (buf ^ 1) * 128, tid, rope_angle(pos_n, s_fhi[tid], s_flo[tid]));
             else if (tid == 64) s_slot[buf ^ 1] = token_slot(a, t + grid, pos_n, req_n);
         }
     }
