@@ -87,6 +87,8 @@ constexpr int kStateRegs = 36;  // per lane and row block: 32 accumulators, m0, 
 constexpr int kMaxLast = 16;    // split units whose merge this CTA owes, held at once
 constexpr int kStageStride = kHeadDim + 4;  // floats per head row of the combiner's staging
 constexpr int kFlyMaxBatch = 1024;  // largest batch whose first descriptor is derived in-kernel
+constexpr int kWalkMaxBatch = 64;   // largest batch whose first bin is walked in-kernel
+constexpr int kWalkTiles = 8;       // tiles streamed on derived descriptors before the map is read
 
 // Warp-uniform bounded wait: lane 0 polls (so all lanes agree on the
 // outcome), then every lane re-observes the completed phase for its own
@@ -203,15 +205,141 @@ __device__ __forceinline__ bool first_descriptor(const AttnParams &p, int c, int
     return true;  // unreachable for a consistent batch
 }
 
+// The descriptors of bin c from the sequence lengths alone, for batches of up
+// to 64 requests (tile counts held in two registers per lane): the closed form
+// of the assign kernel walked unit by unit.  Used by CTAs whose first
+// descriptors are short, so that they need not wait for the assign kernel's
+// map before streaming (its writes become visible to this grid only a few
+// microseconds after that kernel ends).
+struct FlyWalk {
+    int n0, n1;      // tiles of requests lane and lane + 32
+    int N, budget;   // tiles per KV head, tiles per bin
+    long long end;   // global tile where bin c ends
+    int c, k;        // the bin; descriptors produced so far
+    int base;        // index of the bin's first descriptor in the map (-1 until needed)
+    int h, r, pre;   // current unit, tiles of the requests before r
+    long long t;     // global tile at the current descriptor's start
+    int tb, te;      // the current descriptor: tiles [tb, te) of unit (h, r); te == tb: done
+};
+
+__device__ __forceinline__ int walk_tiles(const FlyWalk &w, int r) {
+    return __shfl_sync(kFullMask, r < 32 ? w.n0 : w.n1, r & 31);
+}
+
+__device__ __forceinline__ void walk_init(const AttnParams &p, int c, FlyWalk &w) {
+    const int lane = threadIdx.x & 31, cap = p.max_pages * kTile;
+    int L0 = lane < p.B ? p.seqlens[lane] : 0;
+    int L1 = lane + 32 < p.B ? p.seqlens[lane + 32] : 0;
+    L0 = L0 < 0 ? 0 : min(L0, cap);
+    L1 = L1 < 0 ? 0 : min(L1, cap);
+    w.n0 = (L0 + kTile - 1) / kTile;
+    w.n1 = (L1 + kTile - 1) / kTile;
+    w.N = __reduce_add_sync(kFullMask, w.n0 + w.n1);
+    const long long T = (long long)p.Hkv * w.N;
+    w.budget = (int)max((T + p.num_bins - 1) / p.num_bins, (long long)max(p.min_tiles, 1));
+    w.c = c;
+    w.k = 0;
+    w.base = -1;
+    w.t = (long long)c * w.budget;
+    w.end = min(w.t + w.budget, T);
+    w.h = w.r = w.pre = w.tb = w.te = 0;
+    if (w.t >= T) return;  // an empty bin
+    w.h = (int)(w.t / w.N);
+    const int tl = (int)(w.t - (long long)w.h * w.N);
+    // the request holding tile tl of head h: inclusive prefix over both halves
+    int i0 = w.n0, i1 = w.n1;
+#pragma unroll
+    for (int o_ = 1; o_ < 32; o_ <<= 1) {
+        const int y0 = __shfl_up_sync(kFullMask, i0, o_), y1 = __shfl_up_sync(kFullMask, i1, o_);
+        if (lane >= o_) i0 += y0, i1 += y1;
+    }
+    i1 += __shfl_sync(kFullMask, i0, 31);
+    const unsigned h0 = __ballot_sync(kFullMask, lane < p.B && i0 > tl);
+    const unsigned h1 = __ballot_sync(kFullMask, lane + 32 < p.B && i1 > tl);
+    const int l = h0 ? __ffs(h0) - 1 : 32 + __ffs(h1) - 1;
+    w.r = l;
+    const int incl = __shfl_sync(kFullMask, l < 32 ? i0 : i1, l & 31);
+    const int n = walk_tiles(w, l);
+    w.pre = incl - n;
+    w.tb = tl - w.pre;
+    w.te = w.tb + (int)min((long long)(n - w.tb), w.end - w.t);
+}
+
+// The next descriptor of the bin (te == tb once the bin is done).
+__device__ __forceinline__ void walk_next(const AttnParams &p, FlyWalk &w) {
+    w.t += w.te - w.tb;
+    ++w.k;
+    if (w.t >= w.end) {
+        w.tb = w.te = 0;
+        return;
+    }
+    int n = walk_tiles(w, w.r);
+    do {  // the next unit with tiles (one exists: the bin has tiles left)
+        w.pre += n;
+        if (++w.r == p.B) w.r = 0, w.pre = 0, ++w.h;
+        n = walk_tiles(w, w.r);
+    } while (n == 0);
+    w.tb = 0;
+    w.te = (int)min((long long)n, w.end - w.t);
+}
+
+// The chunk layout of the current descriptor.  Every bin before c holds one
+// descriptor plus one per unit with tiles starting strictly inside it, so the
+// bin's first descriptor has index c + #{such unit starts before tile c *
+// budget}; a unit spans bins first .. last (its chunks, consecutive in the
+// map), and its descriptor in bin c is chunk c - first.
+__device__ __forceinline__ void walk_chunk(const AttnParams &p, FlyWalk &w, int &idx, int &count,
+                                           int &off) {
+    const int lane = threadIdx.x & 31;
+    if (w.base < 0) {
+        int i0 = w.n0, i1 = w.n1;
+#pragma unroll
+        for (int o_ = 1; o_ < 32; o_ <<= 1) {
+            const int y0 = __shfl_up_sync(kFullMask, i0, o_), y1 = __shfl_up_sync(kFullMask, i1, o_);
+            if (lane >= o_) i0 += y0, i1 += y1;
+        }
+        i1 += __shfl_sync(kFullMask, i0, 31);
+        const int e0 = i0 - w.n0, e1 = i1 - w.n1;  // exclusive prefixes
+        const bool a0 = lane < p.B && w.n0 > 0, a1 = lane + 32 < p.B && w.n1 > 0;
+        const long long X = (long long)w.c * w.budget;  // < T, so the loop below ends
+        int inner = 0;
+        if (X <= 0x7FFFFFFFll) {  // 32-bit arithmetic (the common case)
+            const unsigned Xu = (unsigned)X, b = (unsigned)w.budget;
+            for (unsigned hN = 0; hN < Xu; hN += (unsigned)w.N) {
+                const unsigned s0 = hN + e0, s1 = hN + e1;
+                inner += __popc(__ballot_sync(kFullMask, a0 && s0 < Xu && s0 % b != 0)) +
+                         __popc(__ballot_sync(kFullMask, a1 && s1 < Xu && s1 % b != 0));
+            }
+        } else {
+            for (long long hN = 0; hN < X; hN += w.N) {
+                const long long s0 = hN + e0, s1 = hN + e1;
+                inner += __popc(__ballot_sync(kFullMask, a0 && s0 < X && s0 % w.budget != 0)) +
+                         __popc(__ballot_sync(kFullMask, a1 && s1 < X && s1 % w.budget != 0));
+            }
+        }
+        w.base = w.c + inner;
+    }
+    const long long s = (long long)w.h * w.N + w.pre;
+    const int n = walk_tiles(w, w.r);
+    const int first = (int)(s / w.budget), last = (int)((s + n - 1) / w.budget);
+    idx = w.base + w.k;
+    count = last - first + 1;
+    off = idx - (w.c - first);
+}
+
 // Streams one descriptor (h, r, tb, te) through the stage ring.  desc_idx is
-// its index in the task map, or -1 when it is the first descriptor of bin
-// `bin` derived before the map could be read.  Returns false after a timeout.
+// its index in the task map, or -1 when it was derived before the map could
+// be read, as the k-th descriptor of bin `bin`: its chunk layout then comes
+// from `walk` (non-null) or from the map.  The last stage's copies are issued
+// before that layout is looked up (the stage is released once it is written),
+// so a wait for the map overlaps the stage's transfer.  Returns false after a
+// timeout.
 template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                                             const AttnParams &p, uint8_t *smem, int h, int r,
                                             int tb, int te, int desc_idx, int bin,
-                                            ProducerState &ps, uint64_t policy,
-                                            volatile int *abort) {
+                                            FlyWalk *walk, int bin_pos, ProducerState &ps,
+                                            uint64_t policy, volatile int *abort) {
     using Tr = AttnTraits<FP8, STAGES, TPS, NB>;
     const int lane = threadIdx.x & 31;
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Tr::kOffInfo);
@@ -253,15 +381,6 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
 #pragma unroll
             for (int s = 0; s < TPS; ++s) pg[s] = __shfl_sync(kFullMask, page, min(k + s, 31));
             const bool last_stage = t0 + k + ns == te;
-            int idx = desc_idx, count = 0, chunk_off = 0;
-            if (last_stage) {  // the combine step needs the unit's chunk layout
-                wait_for_map(ps);
-                if (idx < 0) idx = p.bin_ptr[bin];
-                if (p.chunk_count) {
-                    count = p.chunk_count[u];
-                    chunk_off = p.chunk_off[u];
-                }
-            }
             const int stage = ps.it % STAGES;
             const uint32_t phase = (ps.it / STAGES) & 1u;
             if (!warp_wait(&empty[stage], phase ^ 1u, abort)) return false;
@@ -275,12 +394,14 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                 si.ntiles = ns;
                 si.flags = (first ? kFirst : 0) | (last_stage ? kLast : 0);
                 si.seqlen = L;
-                si.desc_idx = idx;
-                si.count = count;
-                si.chunk_off = chunk_off;
+                si.desc_idx = desc_idx;
+                si.count = 0;
+                si.chunk_off = 0;
 #pragma unroll
                 for (int g = 0; g < Tr::kRows; ++g) si.qscale[g] = qsg[g];
-                mbar_arrive_expect_tx(&full[stage], 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u));
+                const uint32_t bytes = 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u);
+                if (last_stage) mbar_expect_tx(&full[stage], bytes);  // arrives below
+                else mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
                 for (int s = 0; s < TPS; ++s) {
                     if (s >= ns) break;
@@ -303,6 +424,26 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                     for (int i = 0; i < p.q_len; ++i)
                         bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes + i * q_group,
                                   q_src + i * q_token_stride, q_group, &full[stage]);
+            }
+            if (last_stage) {  // the combine step needs the unit's chunk layout
+                int idx = desc_idx, count = 0, chunk_off = 0;
+                if (idx < 0 && walk) {
+                    walk_chunk(p, *walk, idx, count, chunk_off);
+                } else {
+                    wait_for_map(ps);
+                    if (idx < 0) idx = p.bin_ptr[bin] + bin_pos;
+                    if (p.chunk_count) {
+                        count = p.chunk_count[u];
+                        chunk_off = p.chunk_off[u];
+                    }
+                }
+                if (lane == 0) {
+                    StageInfo &si = info[stage];
+                    si.desc_idx = idx;
+                    si.count = count;
+                    si.chunk_off = chunk_off;
+                    mbar_arrive(&full[stage]);  // releases the stage's fields with it
+                }
             }
             __syncwarp();
             ++ps.it;
@@ -329,12 +470,31 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     // the first bin needs no map: it is derived from the sequence lengths
     // (caller inputs, complete before the assign kernel passed its own wait),
     // so streaming starts at once.
+    // A CTA whose first descriptors are short (the tail of a unit that began
+    // in the bin before) would reach their ends, where the combine needs the
+    // map, long before the map is visible: for batches of up to 64 requests it
+    // walks its bin from the lengths, with the chunk layout derived too, until
+    // kWalkTiles tiles are on their way; the map takes over from there.
     int skip = 0;  // descriptors of the first bin already streamed
-    if (p.fly) {
+    if (p.fly && p.B <= kWalkMaxBatch) {
+        FlyWalk w;
+        walk_init(p, blockIdx.x, w);
+        int streamed = 0;
+        while (ok && w.te > w.tb) {
+            const bool derive = streamed + (w.te - w.tb) < kWalkTiles;
+            ok = stream_desc<FP8, STAGES, TPS, NB>(tmap_k, tmap_v, p, smem, w.h, w.r, w.tb, w.te,
+                                               -1, blockIdx.x, derive ? &w : nullptr, w.k, ps,
+                                               policy, abort);
+            ++skip;
+            streamed += w.te - w.tb;
+            if (!derive) break;  // its end read the map
+            walk_next(p, w);
+        }
+    } else if (p.fly) {
         int h, r, tb, te;
         if (first_descriptor(p, blockIdx.x, h, r, tb, te) && te > tb) {
             ok = stream_desc<FP8, STAGES, TPS, NB>(tmap_k, tmap_v, p, smem, h, r, tb, te, -1,
-                                               blockIdx.x, ps, policy, abort);
+                                               blockIdx.x, nullptr, 0, ps, policy, abort);
             skip = 1;
         }
     }
@@ -353,7 +513,7 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
         for (int d = d_begin; d < d_end && ok; ++d) {
             const int4 ds = p.desc[d];
             ok = stream_desc<FP8, STAGES, TPS, NB>(tmap_k, tmap_v, p, smem, ds.x, ds.y, ds.z, ds.w, d,
-                                               bin, ps, policy, abort);
+                                               bin, nullptr, 0, ps, policy, abort);
         }
         if (!dynamic) break;
         grab = __shfl_sync(kFullMask, grab, 0);

@@ -10,10 +10,12 @@ properties of the rule checked directly on the produced map.
 import os
 import random
 
+import numpy as np
 import pytest
 
 import oracle
 from oracle import assign_closed_form, assign_simulate, static_plan
+from oracle.assign import budget_of, tiles_of
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "assign_tiny.txt")
 
@@ -207,3 +209,69 @@ def test_static_plan_properties():
                 assert nonempty[-1] <= nonempty[0]
                 # fixed split count: the chunk is the smallest that covers n in S pieces
                 assert nonempty[0] * S >= n and (nonempty[0] - 1) * S < n
+
+
+def bin_from_lengths(seqlens, hkv, ctas, floor, c):
+    """Bin c's descriptors with their map indices and chunk layouts, from the
+    lengths alone, by the identities the attention kernel uses before the
+    assign kernel's map is visible: every bin before c holds one descriptor
+    plus one per unit with tiles starting strictly inside it, so bin c's first
+    descriptor is c + #(such starts before tile c * budget); a unit spans bins
+    first .. last, its chunks consecutive in the map, and its descriptor in
+    bin c is chunk c - first."""
+    n = [tiles_of(L) for L in seqlens]
+    N = sum(n)
+    T = hkv * N
+    b = budget_of(T, ctas, floor)
+    X = c * b
+    if X >= T:
+        return []
+    pre = [sum(n[:r]) for r in range(len(n))]
+    starts = [h * N + pre[r] for h in range(hkv) for r in range(len(n)) if n[r] > 0]
+    base = c + sum(1 for s in starts if s < X and s % b != 0)
+    out, t, end = [], X, min(X + b, T)
+    h, tl = divmod(t, N)
+    r = next(i for i in range(len(n)) if pre[i] + n[i] > tl)
+    tb = tl - pre[r]
+    while t < end:
+        te = tb + min(n[r] - tb, end - t)
+        s = h * N + pre[r]
+        first, last = s // b, (s + n[r] - 1) // b
+        idx = base + len(out)
+        out.append(((h, r, tb, te), idx, last - first + 1, idx - (c - first)))
+        t += te - tb
+        while t < end:
+            r += 1
+            if r == len(n):
+                r, h = 0, h + 1
+            if n[r] > 0:
+                break
+        tb = 0
+    return out
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_a_bin_follows_from_the_lengths_alone(seed):
+    """The identities hold on random batches: each bin's descriptors, their
+    indices in the map and their units' chunk counts and first chunks equal
+    the closed-form map's (empty requests, floors and bins past the last
+    tile included)."""
+    rng = np.random.default_rng(4000 + seed)
+    B = int(rng.integers(1, 65))
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    ctas = int(rng.choice([8, 37, 132, 152]))
+    floor = int(rng.choice([1, 2, 5]))
+    seqlens = [int(x) for x in rng.integers(0, 3000, B)]
+    if seed % 3 == 0:
+        seqlens[int(rng.integers(0, B))] = int(rng.integers(20000, 140000))
+    if seed % 5 == 0:
+        seqlens = [0 if rng.random() < 0.3 else L for L in seqlens]
+    tm = assign_closed_form(seqlens, hkv, ctas, floor)
+    for c in range(ctas):
+        got = bin_from_lengths(seqlens, hkv, ctas, floor, c)
+        want = []
+        for d in range(tm.bin_ptr[c], tm.bin_ptr[c + 1]):
+            h, r, tb, te = tm.desc[d]
+            u = h * B + r
+            want.append(((h, r, tb, te), d, tm.chunk_count[u], tm.chunk_off[u]))
+        assert got == want, (c, got, want)
