@@ -44,6 +44,33 @@ def test_small_shapes(kv_dtype, hq, hkv, ctas, fused):
     assert_close(out, oracle_out(batch), kv_dtype)
 
 
+WALK_CASES = [  # (B, Hkv, persistent CTAs, floor): up to 64 requests the first bin is walked
+    (64, 1, 152, 1), (65, 1, 152, 1), (64, 4, 97, 2), (40, 2, 37, 1), (17, 8, 152, 3), (3, 1, 152, 1)]
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("case", range(len(WALK_CASES)))
+def test_first_bins_derived_from_the_lengths(kv_dtype, case):
+    """Mixed lengths with empty requests and a few long ones, so that many
+    bins open with the short tail of a unit that began in the bin before:
+    the CTAs stream their first bins before the task map is visible (walked
+    from the lengths for up to 64 requests, the first descriptor only above).
+    The map and the output match the oracles, the unit counters return to 0."""
+    B, hkv, ctas, floor = WALK_CASES[case]
+    rng = np.random.default_rng(3100 + case)
+    lens = [int(x) for x in rng.integers(1, 1500, B)]
+    for i in rng.choice(B, max(1, B // 8), replace=False):
+        lens[int(i)] = 0
+    for i in rng.choice(B, max(1, B // 16), replace=False):
+        lens[int(i)] = int(rng.integers(8000, 40000))
+    w = Workload(f"walk{case}", B, 8 * hkv, hkv, seqlens=tuple(lens), kv_dtype=kv_dtype,
+                 seed=3200 + case, min_tiles=floor, num_ctas=ctas)
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    out, ws = run_step(batch)
+    assert_map_matches(ws, batch.seqlens.tolist(), hkv, ctas, floor)
+    assert_close(out, oracle_out(batch), kv_dtype)
+
+
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 def test_fused_and_separate_combine_agree(kv_dtype):
     lens = [9000, 3, 64, 700, 129, 20000, 0, 65]
