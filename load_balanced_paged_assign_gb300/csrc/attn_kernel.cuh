@@ -226,6 +226,47 @@ __device__ __forceinline__ int walk_tiles(const FlyWalk &w, int r) {
     return __shfl_sync(kFullMask, r < 32 ? w.n0 : w.n1, r & 31);
 }
 
+// Index in the map of bin c's first descriptor: every bin before c holds one
+// descriptor plus one per unit with tiles starting strictly inside it.
+__device__ __forceinline__ void walk_base(const AttnParams &p, FlyWalk &w) {
+    const int lane = threadIdx.x & 31;
+    int i0 = w.n0, i1 = w.n1;
+#pragma unroll
+    for (int o_ = 1; o_ < 32; o_ <<= 1) {
+        const int y0 = __shfl_up_sync(kFullMask, i0, o_), y1 = __shfl_up_sync(kFullMask, i1, o_);
+        if (lane >= o_) i0 += y0, i1 += y1;
+    }
+    i1 += __shfl_sync(kFullMask, i0, 31);
+    const int e0 = i0 - w.n0, e1 = i1 - w.n1;  // exclusive prefixes
+    const bool a0 = lane < p.B && w.n0 > 0, a1 = lane + 32 < p.B && w.n1 > 0;
+    const long long X = (long long)w.c * w.budget;  // < T: at most Hkv heads below
+    int inner = 0;
+    if (X <= 0x7FFFFFFFll) {
+        // the starts h N + e of each head, their residues mod budget
+        // carried from head to head (one add and compare each): few
+        // instructions, as this runs before the CTA's first copy
+        const unsigned Xu = (unsigned)X, b = (unsigned)w.budget, N = (unsigned)w.N;
+        const unsigned Nm = N % b;
+        unsigned m0 = (unsigned)e0 % b, m1 = (unsigned)e1 % b;
+        int cnt = 0;
+        for (unsigned hN = 0; hN < Xu; hN += N) {
+            cnt += (a0 && hN + e0 < Xu && m0 != 0) + (a1 && hN + e1 < Xu && m1 != 0);
+            m0 += Nm;
+            m0 -= m0 >= b ? b : 0u;
+            m1 += Nm;
+            m1 -= m1 >= b ? b : 0u;
+        }
+        inner = __reduce_add_sync(kFullMask, cnt);
+    } else {
+        for (long long hN = 0; hN < X; hN += w.N) {
+            const long long s0 = hN + e0, s1 = hN + e1;
+            inner += __popc(__ballot_sync(kFullMask, a0 && s0 < X && s0 % w.budget != 0)) +
+                     __popc(__ballot_sync(kFullMask, a1 && s1 < X && s1 % w.budget != 0));
+        }
+    }
+    w.base = w.c + inner;
+}
+
 __device__ __forceinline__ void walk_init(const AttnParams &p, int c, FlyWalk &w) {
     const int lane = threadIdx.x & 31, cap = p.max_pages * kTile;
     int L0 = lane < p.B ? p.seqlens[lane] : 0;
@@ -263,6 +304,7 @@ __device__ __forceinline__ void walk_init(const AttnParams &p, int c, FlyWalk &w
     w.pre = incl - n;
     w.tb = tl - w.pre;
     w.te = w.tb + (int)min((long long)(n - w.tb), w.end - w.t);
+    if (w.te - w.tb < kWalkTiles) walk_base(p, w);  // its layout is derived: index the bin now
 }
 
 // The next descriptor of the bin (te == tb once the bin is done).
@@ -290,38 +332,17 @@ __device__ __forceinline__ void walk_next(const AttnParams &p, FlyWalk &w) {
 // map), and its descriptor in bin c is chunk c - first.
 __device__ __forceinline__ void walk_chunk(const AttnParams &p, FlyWalk &w, int &idx, int &count,
                                            int &off) {
-    const int lane = threadIdx.x & 31;
-    if (w.base < 0) {
-        int i0 = w.n0, i1 = w.n1;
-#pragma unroll
-        for (int o_ = 1; o_ < 32; o_ <<= 1) {
-            const int y0 = __shfl_up_sync(kFullMask, i0, o_), y1 = __shfl_up_sync(kFullMask, i1, o_);
-            if (lane >= o_) i0 += y0, i1 += y1;
-        }
-        i1 += __shfl_sync(kFullMask, i0, 31);
-        const int e0 = i0 - w.n0, e1 = i1 - w.n1;  // exclusive prefixes
-        const bool a0 = lane < p.B && w.n0 > 0, a1 = lane + 32 < p.B && w.n1 > 0;
-        const long long X = (long long)w.c * w.budget;  // < T, so the loop below ends
-        int inner = 0;
-        if (X <= 0x7FFFFFFFll) {  // 32-bit arithmetic (the common case)
-            const unsigned Xu = (unsigned)X, b = (unsigned)w.budget;
-            for (unsigned hN = 0; hN < Xu; hN += (unsigned)w.N) {
-                const unsigned s0 = hN + e0, s1 = hN + e1;
-                inner += __popc(__ballot_sync(kFullMask, a0 && s0 < Xu && s0 % b != 0)) +
-                         __popc(__ballot_sync(kFullMask, a1 && s1 < Xu && s1 % b != 0));
-            }
-        } else {
-            for (long long hN = 0; hN < X; hN += w.N) {
-                const long long s0 = hN + e0, s1 = hN + e1;
-                inner += __popc(__ballot_sync(kFullMask, a0 && s0 < X && s0 % w.budget != 0)) +
-                         __popc(__ballot_sync(kFullMask, a1 && s1 < X && s1 % w.budget != 0));
-            }
-        }
-        w.base = w.c + inner;
-    }
+    if (w.base < 0) walk_base(p, w);
     const long long s = (long long)w.h * w.N + w.pre;
     const int n = walk_tiles(w, w.r);
-    const int first = (int)(s / w.budget), last = (int)((s + n - 1) / w.budget);
+    int first, last;
+    if (s + n <= 0x7FFFFFFFll) {
+        first = (int)((unsigned)s / (unsigned)w.budget);
+        last = (int)((unsigned)(s + n - 1) / (unsigned)w.budget);
+    } else {
+        first = (int)(s / w.budget);
+        last = (int)((s + n - 1) / w.budget);
+    }
     idx = w.base + w.k;
     count = last - first + 1;
     off = idx - (w.c - first);
@@ -330,10 +351,10 @@ __device__ __forceinline__ void walk_chunk(const AttnParams &p, FlyWalk &w, int 
 // Streams one descriptor (h, r, tb, te) through the stage ring.  desc_idx is
 // its index in the task map, or -1 when it was derived before the map could
 // be read, as the k-th descriptor of bin `bin`: its chunk layout then comes
-// from `walk` (non-null) or from the map.  The last stage's copies are issued
-// before that layout is looked up (the stage is released once it is written),
-// so a wait for the map overlaps the stage's transfer.  Returns false after a
-// timeout.
+// from `walk` (non-null: derived, a few instructions) or from the map, in
+// which case its last stage's copies are issued before the map is waited for
+// (the stage is released once the layout is written), so the wait overlaps
+// the stage's transfer.  Returns false after a timeout.
 template <bool FP8, int STAGES, int TPS, int NB>
 __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUtensorMap *tmap_v,
                                             const AttnParams &p, uint8_t *smem, int h, int r,
@@ -381,6 +402,22 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
 #pragma unroll
             for (int s = 0; s < TPS; ++s) pg[s] = __shfl_sync(kFullMask, page, min(k + s, 31));
             const bool last_stage = t0 + k + ns == te;
+            // the combine step needs the unit's chunk layout with the last
+            // stage: read from the map ahead of the stage's wait, or (a
+            // descriptor derived before the map was read) looked up once the
+            // stage's copies are on their way
+            const bool defer = last_stage && desc_idx < 0 && !walk && !ps.waited;
+            int idx = desc_idx, count = 0, chunk_off = 0;
+            if (last_stage && walk) {
+                walk_chunk(p, *walk, idx, count, chunk_off);
+            } else if (last_stage && !defer) {
+                wait_for_map(ps);
+                if (idx < 0) idx = p.bin_ptr[bin] + bin_pos;
+                if (p.chunk_count) {
+                    count = p.chunk_count[u];
+                    chunk_off = p.chunk_off[u];
+                }
+            }
             const int stage = ps.it % STAGES;
             const uint32_t phase = (ps.it / STAGES) & 1u;
             if (!warp_wait(&empty[stage], phase ^ 1u, abort)) return false;
@@ -394,13 +431,13 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                 si.ntiles = ns;
                 si.flags = (first ? kFirst : 0) | (last_stage ? kLast : 0);
                 si.seqlen = L;
-                si.desc_idx = desc_idx;
-                si.count = 0;
-                si.chunk_off = 0;
+                si.desc_idx = idx;
+                si.count = count;
+                si.chunk_off = chunk_off;
 #pragma unroll
                 for (int g = 0; g < Tr::kRows; ++g) si.qscale[g] = qsg[g];
                 const uint32_t bytes = 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u);
-                if (last_stage) mbar_expect_tx(&full[stage], bytes);  // arrives below
+                if (defer) mbar_expect_tx(&full[stage], bytes);  // arrives below
                 else mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
                 for (int s = 0; s < TPS; ++s) {
@@ -425,17 +462,12 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                         bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes + i * q_group,
                                   q_src + i * q_token_stride, q_group, &full[stage]);
             }
-            if (last_stage) {  // the combine step needs the unit's chunk layout
-                int idx = desc_idx, count = 0, chunk_off = 0;
-                if (idx < 0 && walk) {
-                    walk_chunk(p, *walk, idx, count, chunk_off);
-                } else {
-                    wait_for_map(ps);
-                    if (idx < 0) idx = p.bin_ptr[bin] + bin_pos;
-                    if (p.chunk_count) {
-                        count = p.chunk_count[u];
-                        chunk_off = p.chunk_off[u];
-                    }
+            if (defer) {
+                wait_for_map(ps);
+                idx = p.bin_ptr[bin] + bin_pos;
+                if (p.chunk_count) {
+                    count = p.chunk_count[u];
+                    chunk_off = p.chunk_off[u];
                 }
                 if (lane == 0) {
                     StageInfo &si = info[stage];
@@ -476,6 +508,8 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     // walks its bin from the lengths, with the chunk layout derived too, until
     // kWalkTiles tiles are on their way; the map takes over from there.
     int skip = 0;  // descriptors of the first bin already streamed
+    const bool dynamic = p.num_bins > (int)gridDim.x;
+    bool walked = false;  // the whole first bin came from the walk (the map is not needed)
     if (p.fly && p.B <= kWalkMaxBatch) {
         FlyWalk w;
         walk_init(p, blockIdx.x, w);
@@ -490,6 +524,7 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
             if (!derive) break;  // its end read the map
             walk_next(p, w);
         }
+        walked = ok && w.te == w.tb && !ps.waited && !dynamic;
     } else if (p.fly) {
         int h, r, tb, te;
         if (first_descriptor(p, blockIdx.x, h, r, tb, te) && te > tb) {
@@ -498,14 +533,13 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
             skip = 1;
         }
     }
-    wait_for_map(ps);
+    if (!walked) wait_for_map(ps);
 
     // Bins: CTA c starts with bin c; with more bins than CTAs the rest are
     // pulled in order from a device counter (the grab for the following bin
     // is issued when a bin starts, so its latency hides behind the stream).
-    const bool dynamic = p.num_bins > (int)gridDim.x;
     int bin = blockIdx.x;
-    while (ok) {
+    while (ok && !walked) {
         int grab = 0;
         if (dynamic && lane == 0) grab = atomicAdd(p.bin_counter, 1);
         const int d_begin = p.bin_ptr[bin] + (bin == (int)blockIdx.x ? skip : 0);
@@ -535,7 +569,10 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     }
     if (!ok) ps.late_flags |= HPC_FLAG_TIMEOUT;
     const unsigned flags = __reduce_or_sync(kFullMask, ps.late_flags);
-    if (flags && lane == 0) atomicOr(p.meta + 3, (int)flags);
+    if (flags) {
+        wait_for_map(ps);  // meta[3] is written by the assign kernel
+        if (lane == 0) atomicOr(p.meta + 3, (int)flags);
+    }
     // Before leaving, make sure no copy this warp issued is still in flight
     // (bounded as well): the last phase issued on every stage must complete.
     if (lane == 0) {
