@@ -67,7 +67,8 @@ def test_scores_against_the_oracle(M):
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (200, 272, 128), (129, 256, 4096),
                                    (3, 192, 4096), (700, 64, 1024), (77, 176, 512),
                                    (1000, 48, 256), (4100, 192, 4096), (40, 16, 128),
-                                   (5000, 48, 1024), (2000, 512, 512)])
+                                   (5000, 48, 1024), (2000, 512, 512), (8, 192, 4096),
+                                   (12, 64, 1024), (9, 16, 128), (16, 192, 8192)])
 def test_other_shapes(M, N, K):
     x, w = make_router_inputs(M, K=K, N=N, seed=1500 + M + N, device="cuda")
     hi, lo = split_gpu(w)
