@@ -655,7 +655,10 @@ __device__ __forceinline__ void merge_unit_rows(const AttnParams &p, const DescI
     const float4 *po[K];
     float wl[K], wsum[K], m[K];
     float4 acc[K];
+    float4 x[K][MB];
     int maxc = 0;
+    // first round: every row's LSEs and its first MB chunk rows together (the
+    // rows do not depend on the weights)
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         po[k] = reinterpret_cast<const float4 *>(p.part_o +
@@ -665,6 +668,10 @@ __device__ __forceinline__ void merge_unit_rows(const AttnParams &p, const DescI
         wl[k] = lane < di[k].count ? __ldcg(lse + (size_t)lane * p.R) : kNegInf;
         maxc = max(maxc, di[k].count);
         acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < MB; ++j)
+            x[k][j] = j < di[k].count ? __ldcg(po[k] + (size_t)j * row)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -677,13 +684,14 @@ __device__ __forceinline__ void merge_unit_rows(const AttnParams &p, const DescI
         for (int o_ = 16; o_ > 0; o_ >>= 1) wsum[k] += __shfl_xor_sync(kFullMask, wsum[k], o_);
     }
     for (int i0 = 0; i0 < maxc; i0 += MB) {
-        float4 x[K][MB];
+        if (i0 > 0) {
 #pragma unroll
-        for (int k = 0; k < K; ++k)
+            for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < MB; ++j)
-                x[k][j] = i0 + j < di[k].count ? __ldcg(po[k] + (size_t)(i0 + j) * row)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < MB; ++j)
+                    x[k][j] = i0 + j < di[k].count ? __ldcg(po[k] + (size_t)(i0 + j) * row)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
@@ -1229,7 +1237,7 @@ __global__ void __launch_bounds__(AttnTraits<FP8, STAGES, TPS, NB>::kThreads, 1)
                 if (d0.count <= 32 && d1.count <= 32) {
                     const DescInfo dd[2] = {d0, d1};
                     const int rr[2] = {item % p.R, (item + 1) % p.R};
-                    merge_unit_rows<8, 2>(p, dd, rr);
+                    merge_unit_rows<12, 2>(p, dd, rr);
                 } else {
                     merge_unit_head<NB == 1 ? 16 : 8>(p, d0, item % p.R);
                     merge_unit_head<NB == 1 ? 16 : 8>(p, d1, (item + 1) % p.R);
