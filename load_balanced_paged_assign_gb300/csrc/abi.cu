@@ -305,9 +305,12 @@ int32_t hpc_decode_num_ctas(int32_t device, hpc_kv_dtype kv_dtype) {
     return sms * per_sm;
 }
 
-hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
-                           int32_t max_pages_per_req, int32_t num_ctas,
-                           int32_t min_tiles_per_cta, hpc_task_map *map, hpc_stream_t stream) {
+namespace {
+// The load-balanced plan; bt_prefetch (the step's block table, or null) is
+// warmed in L2 by the assign kernel for the attention grid that follows.
+hpc_status plan_impl(const int32_t *d_seqlens, int32_t B, int32_t Hkv, int32_t max_pages_per_req,
+                     int32_t num_ctas, int32_t min_tiles_per_cta, hpc_task_map *map,
+                     hpc_stream_t stream, const int32_t *bt_prefetch) {
     if (B < 0 || Hkv <= 0 || max_pages_per_req <= 0 || num_ctas < 1 || min_tiles_per_cta < 0)
         return HPC_ERR_ARG;
     if (min_tiles_per_cta >= (1 << 29)) return HPC_ERR_ARG;
@@ -327,9 +330,18 @@ hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
     m.min_tiles = min_tiles_per_cta;
     m.max_pages = max_pages_per_req;
     st = cuda_status(launch_assign(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
-                                   min_tiles_per_cta, m, static_cast<cudaStream_t>(stream)));
+                                   min_tiles_per_cta, m, static_cast<cudaStream_t>(stream),
+                                   bt_prefetch));
     if (st == HPC_OK) *map = m;
     return st;
+}
+}  // namespace
+
+hpc_status hpc_decode_plan(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
+                           int32_t max_pages_per_req, int32_t num_ctas,
+                           int32_t min_tiles_per_cta, hpc_task_map *map, hpc_stream_t stream) {
+    return plan_impl(d_seqlens, B, Hkv, max_pages_per_req, num_ctas, min_tiles_per_cta, map,
+                     stream, nullptr);
 }
 
 hpc_status hpc_decode_plan_static(const int32_t *d_seqlens, int32_t B, int32_t Hkv,
@@ -439,8 +451,8 @@ hpc_status hpc_decode_step_mq(const void *d_q, const float *d_q_scale, const voi
     if (st != HPC_OK) return st;
     if (num_splits < 0 || q_len < 1) return HPC_ERR_ARG;
     if (q_len * (Hq / Hkv) > HPC_MAX_QUERY_ROWS) return HPC_ERR_UNSUPPORTED;
-    st = num_splits == 0 ? hpc_decode_plan(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
-                                           min_tiles_per_cta, map, stream)
+    st = num_splits == 0 ? plan_impl(d_seqlens, B, Hkv, max_pages_per_req, num_ctas,
+                                     min_tiles_per_cta, map, stream, d_block_table)
                          : hpc_decode_plan_static(d_seqlens, B, Hkv, max_pages_per_req,
                                                   num_splits, map, stream);
     if (st != HPC_OK) return st;

@@ -65,8 +65,11 @@ cudaError_t launch_attn_bf16(int nb, const CUtensorMap &tk, const CUtensorMap &t
 cudaError_t launch_attn_fp8(int nb, const CUtensorMap &tk, const CUtensorMap &tv,
                             const AttnParams &p, int grid, cudaStream_t s);
 
+// bt_prefetch (or null): a block table [B, max_pages] the kernel warms in L2
+// for the attention grid that follows it.
 cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages, int num_ctas,
-                          int floor, const hpc_task_map &map, cudaStream_t s);
+                          int floor, const hpc_task_map &map, cudaStream_t s,
+                          const int32_t *bt_prefetch = nullptr);
 cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_pages,
                                int num_splits, const hpc_task_map &map, cudaStream_t s);
 int assign_smem_bytes(int B);

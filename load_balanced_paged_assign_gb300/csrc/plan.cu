@@ -61,17 +61,28 @@ __device__ __forceinline__ int live_len(const int32_t *seqlens, int r, int max_p
     return L;
 }
 
+constexpr size_t kPrefetchMaxBytes = 4u << 20;  // block-table bytes warmed in L2 at most
+
 __global__ void __launch_bounds__(kPlanThreads)
     assign_kernel(const int32_t *__restrict__ seqlens, int B, int Hkv, int max_pages,
                   int num_ctas, int floor, int4 *__restrict__ desc, int32_t *__restrict__ bin_ptr,
                   int32_t *__restrict__ chunk_count, int32_t *__restrict__ chunk_off,
-                  int32_t *__restrict__ meta, int cap_desc) {
+                  int32_t *__restrict__ meta, int cap_desc, const int32_t *bt_prefetch) {
     extern __shared__ int s_end[];  // [B] inclusive prefix of tiles per request
     __shared__ int s_scan[32];
     __shared__ unsigned s_flags;
     const int tid = threadIdx.x;
     grid_dependency_wait();    // launched as a dependent: the previous grid is done
     grid_launch_dependents();  // the attention grid may start its prologue now
+    if (bt_prefetch) {
+        // the step's block table into L2 (no registers held, nothing waited
+        // for): the attention grid looks up the pages of its first tiles
+        // while this kernel still runs
+        const size_t bytes = min((size_t)B * max_pages * 4, kPrefetchMaxBytes);
+        const char *bt = reinterpret_cast<const char *>(bt_prefetch);
+        for (size_t off = (size_t)tid * 128; off < bytes; off += (size_t)blockDim.x * 128)
+            prefetch_l2(bt + off);
+    }
     if (tid == 0) s_flags = 0;
     unsigned flags = 0;
 
@@ -208,7 +219,8 @@ static int plan_threads(int B, int Hkv, int num_ctas) {
 }
 
 cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages, int num_ctas,
-                          int floor, const hpc_task_map &map, cudaStream_t s) {
+                          int floor, const hpc_task_map &map, cudaStream_t s,
+                          const int32_t *bt_prefetch) {
     const int smem = assign_smem_bytes(B);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(assign_kernel,
@@ -227,7 +239,7 @@ cudaError_t launch_assign(const int32_t *seqlens, int B, int Hkv, int max_pages,
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, assign_kernel, seqlens, B, Hkv, max_pages, num_ctas, floor,
                               reinterpret_cast<int4 *>(map.desc), map.bin_ptr, map.chunk_count,
-                              map.chunk_off, map.meta, map.cap_desc);
+                              map.chunk_off, map.meta, map.cap_desc, bt_prefetch);
 }
 
 cudaError_t launch_static_plan(const int32_t *seqlens, int B, int Hkv, int max_pages,
