@@ -359,7 +359,11 @@ int64_t hpc_decode_packed_layout(int32_t B, int32_t Hq, int32_t max_pages_per_re
  * asynchronous): one host-to-device copy into the caller's device staging
  * buffer d_in (same size, 16-byte aligned), the step on the device sections,
  * and one device-to-host copy of d_out into h_out.  The same bytes move as
- * with the separate buffers, in one transfer each way.
+ * with the separate buffers, in one transfer each way.  With d_out NULL (and
+ * d_unit_done given: the combine fused into the attention grid) the kernels
+ * store the BF16 output straight into h_out, which must then be pinned host
+ * memory with a device alias (cudaHostAlloc memory under unified addressing;
+ * HPC_ERR_ARG otherwise): no separate copy out.
  */
 hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out, void *d_out,
                                        const void *d_k_cache, const void *d_v_cache,

@@ -560,8 +560,25 @@ hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out
     int64_t off[4];
     const int64_t bytes = hpc_decode_packed_layout(B, Hq, max_pages_per_req, kv_dtype, off);
     if (bytes < 0) return HPC_ERR_ARG;
-    if (B > 0 && (!h_in || !d_in || !h_out || !d_out)) return HPC_ERR_ARG;
+    if (B > 0 && (!h_in || !d_in || !h_out)) return HPC_ERR_ARG;
+    if (B > 0 && !d_out && !d_unit_done) return HPC_ERR_ARG;  // direct output needs the fused combine
     if (B > 0 && !aligned16(d_in)) return HPC_ERR_ARG;
+    // d_out null: the attention grid (combine fused) stores the output straight
+    // into h_out through its device alias (pinned host memory under unified
+    // addressing), with no separate copy
+    void *out = d_out;
+    const bool to_host = B > 0 && d_out == nullptr;
+    if (to_host) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, h_out) != cudaSuccess) {
+            cudaGetLastError();
+            return HPC_ERR_ARG;
+        }
+        if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr ||
+            !aligned16(pa.devicePointer))
+            return HPC_ERR_ARG;
+        out = pa.devicePointer;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
     char *d = static_cast<char *>(d_in);
@@ -572,8 +589,8 @@ hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out
                          reinterpret_cast<const int32_t *>(d + off[3]), max_pages_per_req,
                          reinterpret_cast<const int32_t *>(d + off[2]), B, Hq, Hkv, head_dim,
                          sm_scale, num_ctas, min_tiles_per_cta, num_splits, map, d_part_o,
-                         d_part_lse, d_unit_done, d_out, stream);
-    if (st != HPC_OK || B == 0) return st;
+                         d_part_lse, d_unit_done, out, stream);
+    if (st != HPC_OK || B == 0 || to_host) return st;
     return cuda_status(cudaMemcpyAsync(h_out, d_out, (size_t)B * Hq * HPC_HEAD_DIM * 2,
                                        cudaMemcpyDeviceToHost, s));
 }

@@ -281,12 +281,16 @@ def test_packed_step_argument_checks(hd):
     E = hd.binding
     m = E.hpc_task_map()
 
-    def call(h_in=FAKE, d_in=FAKE, h_out=FAKE, d_out=FAKE, B=4, D=128):
+    def call(h_in=FAKE, d_in=FAKE, h_out=FAKE, d_out=FAKE, B=4, D=128, unit_done=FAKE):
         return L.hpc_decode_step_host_packed(h_in, d_in, h_out, d_out, FAKE, FAKE, 100, 1.0, 1.0,
                                              0, 8, B, 8, 1, D, 0.088, 132, 2, 0,
-                                             ctypes.byref(m), FAKE, FAKE, FAKE, None)
+                                             ctypes.byref(m), FAKE, FAKE, unit_done, None)
 
     assert call(h_in=None) == E.HPC_ERR_ARG
-    assert call(d_out=None) == E.HPC_ERR_ARG
+    assert call(h_out=None) == E.HPC_ERR_ARG
+    # no device output: the kernels store into h_out, which needs the fused
+    # combine and a device-mapped pinned host buffer
+    assert call(d_out=None, unit_done=None) == E.HPC_ERR_ARG
+    assert call(d_out=None) == E.HPC_ERR_ARG  # FAKE is no registered host memory
     assert call(d_in=FAKE + 8) == E.HPC_ERR_ARG  # device staging not 16-byte aligned
     assert call(D=64) == E.HPC_ERR_UNSUPPORTED

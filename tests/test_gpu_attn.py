@@ -405,3 +405,17 @@ def test_packed_host_step_equals_the_device_step(name):
                                    unit_done=ws.unit_done)
     torch.cuda.synchronize()
     assert torch.equal(h_out.view(torch.int16), ref.cpu().view(torch.int16))
+    # no device output: the kernels store straight into the pinned host buffer
+    h_out2 = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hd.hpc_decode_step_host_packed(h_in, d_in, h_out2, None, batch.k_cache, batch.v_cache,
+                                   batch.k_scale, batch.v_scale, B, Hq, Hkv, mp, w.sm_scale, ctas,
+                                   w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse,
+                                   unit_done=ws.unit_done)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out2.view(torch.int16), ref.cpu().view(torch.int16))
+    # a pageable host buffer has no device alias: refused, nothing launched
+    with pytest.raises(hd.HpcError):
+        hd.hpc_decode_step_host_packed(h_in, d_in, torch.empty((B, Hq, 128), dtype=torch.bfloat16),
+                                       None, batch.k_cache, batch.v_cache, batch.k_scale,
+                                       batch.v_scale, B, Hq, Hkv, mp, w.sm_scale, ctas, w.min_tiles,
+                                       0, ws.tmap, ws.part_o, ws.part_lse, unit_done=ws.unit_done)
