@@ -500,6 +500,17 @@ hpc_status hpc_rope_norm(const void *d_qkv, int64_t qkv_row_stride, const void *
                          void *d_q_out, float *d_q_scale_out, int32_t *d_flags,
                          const hpc_rope_norm_params *params, hpc_stream_t stream);
 
+/*
+ * Self-test of the bounded waits every kernel here relies on (each waits on
+ * a barrier for at most a time limit, then raises HPC_FLAG_TIMEOUT and leaves
+ * instead of hanging): launches one CTA that waits on a shared-memory barrier
+ * nothing completes, with a limit of limit_us microseconds (1 .. 10^6).  When
+ * the limit passes the kernel ORs HPC_FLAG_TIMEOUT into *d_flags (device
+ * int32) and returns; the context stays usable.  HPC_ERR_ARG for a null flag
+ * word or a limit out of range.  Asynchronous on `stream`.
+ */
+hpc_status hpc_selftest_wait_timeout(int32_t *d_flags, int32_t limit_us, hpc_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Router GEMM with FP32 weights on BF16 tensor cores (SGLang post, section
  * "Router GEMM：在路由精度与吞吐量之间取得平衡", and its summary bullet): the

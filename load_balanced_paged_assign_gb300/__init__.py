@@ -20,6 +20,7 @@ from .binding import (EXPORTS, HPC_KV_BF16, HPC_KV_FP8_E4M3, HPC_ROPE_HALVES,
                       hpc_decode_packed_layout, hpc_decode_step_host,
                       hpc_decode_step_host_packed, hpc_decode_version, hpc_prefill_attn,
                       hpc_rope_frequencies, hpc_rope_norm, hpc_router_gemm, hpc_router_plan, hpc_router_split, hpc_router_workspace_bytes,
+                      hpc_selftest_wait_timeout,
                       kv_dtype_of, lib)
 
 __all__ = [
@@ -31,5 +32,6 @@ __all__ = [
     "hpc_decode_packed_layout", "hpc_decode_static_capacity", "hpc_decode_step",
     "hpc_decode_step_host", "hpc_decode_step_host_packed", "hpc_decode_step_mq",
     "hpc_decode_version", "hpc_prefill_attn", "hpc_rope_frequencies", "hpc_rope_norm", "hpc_router_gemm",
-    "hpc_router_plan", "hpc_router_split", "hpc_router_workspace_bytes", "kv_dtype_of", "lib",
+    "hpc_router_plan", "hpc_router_split", "hpc_router_workspace_bytes", "hpc_selftest_wait_timeout",
+    "kv_dtype_of", "lib",
 ]

@@ -28,7 +28,8 @@ EXPORTS = (
     "hpc_decode_attn_combine", "hpc_decode_combine", "hpc_decode_step", "hpc_decode_step_host", "hpc_decode_read_meta",
     "hpc_decode_step_noalloc", "hpc_rope_norm", "hpc_rope_frequencies", "hpc_decode_attn_mq",
     "hpc_decode_attn_combine_mq", "hpc_decode_combine_mq", "hpc_decode_step_mq",
-    "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_plan", "hpc_router_gemm", "hpc_prefill_attn",
+    "hpc_selftest_wait_timeout", "hpc_router_split", "hpc_router_workspace_bytes", "hpc_router_plan",
+    "hpc_router_gemm", "hpc_prefill_attn",
     "hpc_decode_packed_layout", "hpc_decode_step_host_packed",
 )
 
@@ -106,6 +107,7 @@ def lib():
         "hpc_router_split": (ctypes.c_int, [vp, i32, i32, vp, vp, vp]),
         "hpc_router_workspace_bytes": (i64, [i32, i32, i32]),
         "hpc_router_plan": (ctypes.c_int, [i32, i32, i32, vp]),
+        "hpc_selftest_wait_timeout": (ctypes.c_int, [vp, i32, vp]),
         "hpc_router_gemm": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
         "hpc_prefill_attn": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                             i32, f32, vp, vp, vp]),
@@ -335,6 +337,13 @@ def hpc_router_split(w, w_hi, w_lo, stream=None):
 
 def hpc_router_workspace_bytes(M, N, K) -> int:
     return int(lib().hpc_router_workspace_bytes(int(M), int(N), int(K)))
+
+
+def hpc_selftest_wait_timeout(flags, limit_us, stream=None):
+    """One CTA waits on a barrier nothing completes for limit_us, then raises
+    HPC_FLAG_TIMEOUT in flags (device int32) and returns."""
+    _check("hpc_selftest_wait_timeout",
+           lib().hpc_selftest_wait_timeout(_ptr(flags), int(limit_us), _stream(stream)))
 
 
 def hpc_router_plan(M, N, K) -> dict:

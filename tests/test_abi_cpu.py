@@ -294,3 +294,11 @@ def test_packed_step_argument_checks(hd):
     assert call(d_out=None) == E.HPC_ERR_ARG  # FAKE is no registered host memory
     assert call(d_in=FAKE + 8) == E.HPC_ERR_ARG  # device staging not 16-byte aligned
     assert call(D=64) == E.HPC_ERR_UNSUPPORTED
+
+
+def test_selftest_argument_checks(hd):
+    L = hd.lib()
+    E = hd.binding
+    assert L.hpc_selftest_wait_timeout(None, 1000, None) == E.HPC_ERR_ARG
+    assert L.hpc_selftest_wait_timeout(FAKE, 0, None) == E.HPC_ERR_ARG
+    assert L.hpc_selftest_wait_timeout(FAKE, 1000001, None) == E.HPC_ERR_ARG
