@@ -549,7 +549,7 @@ def main():
         d2h = h_out.numel() * 2
         e2e = {"value": max(max_over_ranks(statistics.fmean(tot), world)), "unit": "us/step",
                "h2d_bytes_per_step": total, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "api": "hpc_decode_step_host_packed (one pinned input buffer, one copy each way)",
+               "api": "hpc_decode_step_host_packed (one pinned input buffer copied in; the output stored by the attention grid into pinned host memory)",
                "separate_buffers_us": statistics.fmean(sep),
                "separate_buffers_api": "hpc_decode_step_host (a copy per input array)"}
 
