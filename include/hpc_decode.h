@@ -355,10 +355,13 @@ int64_t hpc_decode_packed_layout(int32_t B, int32_t Hq, int32_t max_pages_per_re
 
 /*
  * hpc_decode_step_host with the per-step inputs in ONE host buffer h_in
- * (the layout of hpc_decode_packed_layout; pinned memory makes the copy
- * asynchronous): one host-to-device copy into the caller's device staging
- * buffer d_in (same size, 16-byte aligned), the step on the device sections,
- * and one device-to-host copy of d_out into h_out.  The same bytes move as
+ * (the layout of hpc_decode_packed_layout) brought into the caller's device
+ * staging buffer d_in (same size, 16-byte aligned), the step on the device
+ * sections, and one device-to-host copy of d_out into h_out.  Pinned h_in
+ * (with a 16-byte-aligned device alias) is read by a copy kernel through its
+ * alias, one 16-byte load per thread, with the assign kernel launched as its
+ * programmatic dependent; pageable h_in goes through the copy engine
+ * (cudaMemcpyAsync, synchronous for pageable memory).  The same bytes move as
  * with the separate buffers, in one transfer each way.  With d_out NULL (and
  * d_unit_done given: the combine fused into the attention grid) the kernels
  * store the BF16 output straight into h_out, which must then be pinned host

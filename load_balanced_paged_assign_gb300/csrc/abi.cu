@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 using namespace hpc;
 
@@ -252,6 +253,34 @@ hpc_status combine_impl(const float *d_part_o, const float *d_part_lse, const hp
     if (map->B != B || map->Hkv != Hkv || (int64_t)B * Hkv > map->cap_units) return HPC_ERR_ARG;
     return cuda_status(launch_combine(d_part_o, d_part_lse, *map, B, Hq, Hkv, q_len, d_out,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+// The packed per-step inputs, from pinned host memory read through its device
+// alias into the device buffer: one 16-byte load per thread, so the transfer
+// is a single round trip over the CPU-GPU link.  It lets the grid after it
+// (the assign kernel, a programmatic dependent that reads nothing before
+// griddepcontrol.wait) launch at once instead of behind a copy-engine
+// transfer.  Launched as an ordinary kernel: the previous step's grids may
+// still read the device buffer until they end.
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_in_kernel(const int4 *__restrict__ src,
+                                                               int4 *__restrict__ dst, int64_t n) {
+    grid_launch_dependents();
+    for (int64_t i = (int64_t)blockIdx.x * kCopyThreads + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * kCopyThreads)
+        dst[i] = src[i];
+}
+
+// The device alias of a pinned (page-locked, mapped) host buffer, or null for
+// pageable memory.
+const void *host_alias(const void *h) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
 }
 
 }  // namespace
@@ -569,21 +598,26 @@ hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out
     void *out = d_out;
     const bool to_host = B > 0 && d_out == nullptr;
     if (to_host) {
-        cudaPointerAttributes pa;
-        if (cudaPointerGetAttributes(&pa, h_out) != cudaSuccess) {
-            cudaGetLastError();
-            return HPC_ERR_ARG;
-        }
-        if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr ||
-            !aligned16(pa.devicePointer))
-            return HPC_ERR_ARG;
-        out = pa.devicePointer;
+        out = const_cast<void *>(host_alias(h_out));
+        if (!out || !aligned16(out)) return HPC_ERR_ARG;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
     char *d = static_cast<char *>(d_in);
-    if (B > 0 && cudaMemcpyAsync(d_in, h_in, (size_t)bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return HPC_ERR_CUDA;
+    if (B > 0) {
+        // pinned input: copied by copy_in_kernel; pageable: by the copy engine
+        const void *src = host_alias(h_in);
+        if (src && aligned16(src)) {
+            const int64_t n = bytes / 16;  // the layout's size is a multiple of 16
+            const int grid = (int)std::min<int64_t>((n + kCopyThreads - 1) / kCopyThreads, 1024);
+            copy_in_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const int4 *>(src),
+                                                          static_cast<int4 *>(d_in), n);
+            if (cudaGetLastError() != cudaSuccess) return HPC_ERR_CUDA;
+        } else if (cudaMemcpyAsync(d_in, h_in, (size_t)bytes, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess) {
+            return HPC_ERR_CUDA;
+        }
+    }
     st = hpc_decode_step(d + off[0], fp8 ? reinterpret_cast<const float *>(d + off[1]) : nullptr,
                          d_k_cache, d_v_cache, num_pages, k_scale, v_scale, kv_dtype,
                          reinterpret_cast<const int32_t *>(d + off[3]), max_pages_per_req,

@@ -379,8 +379,10 @@ def test_table4_decode_rows(name):
 
 @pytest.mark.parametrize("name", ["hy3_tp8", "fp8"])
 def test_packed_host_step_equals_the_device_step(name):
-    """hpc_decode_step_host_packed: one pinned input buffer, one copy each way;
-    the output is bit-identical to the device-buffer step on the same inputs."""
+    """hpc_decode_step_host_packed: one input buffer brought in (a pinned one
+    by a copy kernel through its device alias, a pageable one by the copy
+    engine); the output, in a device buffer copied out or stored straight into
+    pinned host memory, is bit-identical to the device-buffer step."""
     w = WORKLOADS[name]
     batch = make_batch(w, device="cuda")
     ref, _ = run_step(batch)
@@ -413,7 +415,20 @@ def test_packed_host_step_equals_the_device_step(name):
                                    unit_done=ws.unit_done)
     torch.cuda.synchronize()
     assert torch.equal(h_out2.view(torch.int16), ref.cpu().view(torch.int16))
-    # a pageable host buffer has no device alias: refused, nothing launched
+    assert torch.equal(d_in.cpu(), h_in)  # every byte of the pinned input arrived
+    # a pageable input buffer goes through the copy engine: the same output
+    h_pageable = torch.empty(total, dtype=torch.uint8)
+    h_pageable.copy_(h_in)
+    assert not h_pageable.is_pinned()
+    d_in.zero_()
+    h_out3 = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hd.hpc_decode_step_host_packed(h_pageable, d_in, h_out3, None, batch.k_cache, batch.v_cache,
+                                   batch.k_scale, batch.v_scale, B, Hq, Hkv, mp, w.sm_scale, ctas,
+                                   w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse,
+                                   unit_done=ws.unit_done)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out3.view(torch.int16), ref.cpu().view(torch.int16))
+    # a pageable output buffer has no device alias: refused, nothing launched
     with pytest.raises(hd.HpcError):
         hd.hpc_decode_step_host_packed(h_in, d_in, torch.empty((B, Hq, 128), dtype=torch.bfloat16),
                                        None, batch.k_cache, batch.v_cache, batch.k_scale,
