@@ -551,7 +551,7 @@ def main():
                "h2d_bytes_per_step": total, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "api": "hpc_decode_step_host_packed (one pinned input buffer copied in; the output stored by the attention grid into pinned host memory)",
                "separate_buffers_us": statistics.fmean(sep),
-               "separate_buffers_api": "hpc_decode_step_host (a copy per input array)"}
+               "separate_buffers_api": "hpc_decode_step_host (one copy kernel over the pinned input arrays; the output copied out by the copy engine)"}
 
     # ---- in-house static split-KV comparator on the same batch
     static = None

@@ -324,12 +324,17 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
                            int32_t *d_unit_done, void *d_out, hpc_stream_t stream);
 
 /*
- * hpc_decode_step with the per-step inputs and the output in host memory
- * (pinned memory makes the copies asynchronous): copies h_q, h_q_scale
- * (FP8 only), h_seqlens and h_block_table into the caller's device staging
- * buffers d_q, d_q_scale, d_seqlens, d_block_table, runs the step, and copies
- * d_out back into h_out.  The KV caches stay device-resident, as they are
- * in serving.  The host output is complete once `stream` has finished.
+ * hpc_decode_step with the per-step inputs and the output in host memory:
+ * brings h_q, h_q_scale (FP8 only), h_seqlens and h_block_table into the
+ * caller's device staging buffers d_q, d_q_scale, d_seqlens, d_block_table,
+ * runs the step, and copies d_out back into h_out.  When every input is
+ * pinned host memory with a device alias, one copy kernel reads them all
+ * through their aliases (16-byte vectors where both addresses are 16-byte
+ * aligned, bytes otherwise) and the assign kernel launches behind it as a
+ * programmatic dependent; otherwise each array is one cudaMemcpyAsync
+ * (synchronous for pageable memory).  The KV caches stay device-resident, as
+ * they are in serving.  The host output is complete once `stream` has
+ * finished.
  */
 hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const int32_t *h_seqlens,
                                 const int32_t *h_block_table, void *h_out, void *d_q,

@@ -272,6 +272,33 @@ __global__ void __launch_bounds__(kCopyThreads) copy_in_kernel(const int4 *__res
         dst[i] = src[i];
 }
 
+// Up to four host arrays copied by one launch (grid row y = array y), each
+// as 16-byte vectors when both ends are 16-byte aligned, else byte by byte.
+struct CopySegments {
+    const char *src[4];
+    char *dst[4];
+    int64_t bytes[4];
+};
+
+__global__ void __launch_bounds__(kCopyThreads) copy_in_segments_kernel(const CopySegments c) {
+    grid_launch_dependents();
+    const int y = blockIdx.y;  // selected without indexing the parameter block
+    const char *src = y == 0 ? c.src[0] : y == 1 ? c.src[1] : y == 2 ? c.src[2] : c.src[3];
+    char *dst = y == 0 ? c.dst[0] : y == 1 ? c.dst[1] : y == 2 ? c.dst[2] : c.dst[3];
+    const int64_t bytes = y == 0 ? c.bytes[0] : y == 1 ? c.bytes[1] : y == 2 ? c.bytes[2] : c.bytes[3];
+    const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
+    const int64_t first = (int64_t)blockIdx.x * kCopyThreads + threadIdx.x;
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t n = bytes / 16;
+        for (int64_t i = first; i < n; i += stride)
+            reinterpret_cast<int4 *>(dst)[i] = reinterpret_cast<const int4 *>(src)[i];
+        done = n * 16;
+    }
+    for (int64_t i = done + first; i < bytes; i += stride) dst[i] = src[i];
+}
+
 // The device alias of a pinned (page-locked, mapped) host buffer, or null for
 // pageable memory.
 const void *host_alias(const void *h) {
@@ -535,17 +562,36 @@ hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const i
     const size_t out_bytes = (size_t)B * Hq * HPC_HEAD_DIM * 2;
     cudaError_t e = cudaSuccess;
     if (B > 0) {
-        e = cudaMemcpyAsync(d_q, h_q, q_bytes, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess && fp8)
-            e = cudaMemcpyAsync(d_q_scale, h_q_scale, (size_t)B * Hq * sizeof(float),
-                                cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(d_seqlens, h_seqlens, (size_t)B * sizeof(int32_t),
-                                cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(d_block_table, h_block_table,
-                                (size_t)B * max_pages_per_req * sizeof(int32_t),
-                                cudaMemcpyHostToDevice, s);
+        // all inputs pinned: one copy kernel reads them through their device
+        // aliases (the assign kernel launches behind it as a programmatic
+        // dependent); otherwise one copy-engine transfer per array
+        const void *hs[4] = {h_q, fp8 ? h_q_scale : nullptr, h_seqlens, h_block_table};
+        void *ds[4] = {d_q, fp8 ? d_q_scale : nullptr, d_seqlens, d_block_table};
+        const int64_t nb[4] = {(int64_t)q_bytes, fp8 ? (int64_t)B * Hq * 4 : 0, (int64_t)B * 4,
+                               (int64_t)B * max_pages_per_req * 4};
+        CopySegments cs = {};
+        int n = 0;
+        int64_t widest = 0;
+        bool pinned = true;
+        for (int i = 0; i < 4 && pinned; ++i) {
+            if (nb[i] == 0) continue;
+            const void *a = host_alias(hs[i]);
+            if (!a) pinned = false;
+            cs.src[n] = static_cast<const char *>(a);
+            cs.dst[n] = static_cast<char *>(ds[i]);
+            cs.bytes[n] = nb[i];
+            widest = std::max(widest, (nb[i] + 15) / 16);
+            ++n;
+        }
+        if (pinned) {
+            const int gx = (int)std::min<int64_t>((widest + kCopyThreads - 1) / kCopyThreads, 1024);
+            copy_in_segments_kernel<<<dim3(gx, n), kCopyThreads, 0, s>>>(cs);
+            e = cudaGetLastError();
+        } else {
+            for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+                if (nb[i] > 0)
+                    e = cudaMemcpyAsync(ds[i], hs[i], (size_t)nb[i], cudaMemcpyHostToDevice, s);
+        }
         if (e != cudaSuccess) return HPC_ERR_CUDA;
     }
     st = hpc_decode_step(d_q, d_q_scale, d_k_cache, d_v_cache, num_pages, k_scale, v_scale,

@@ -218,23 +218,56 @@ def test_bad_page_is_flagged_not_read_out_of_bounds():
     assert_close(out[1:], ref[1:], "bf16")  # the other request is unaffected
 
 
-def test_host_buffer_step_matches_device_step():
-    w = WORKLOADS["tiny"]
+def _host_copy(t, pinned, shift):
+    """A host copy of t: pinned or pageable; shift = 1 places it 4 bytes past a
+    16-byte boundary (int32 / float32 arrays only)."""
+    c = t.cpu().contiguous()
+    if not shift:
+        return c.pin_memory() if pinned else c.clone()
+    flat = torch.empty(c.numel() + 4, dtype=c.dtype)
+    if pinned:
+        flat = flat.pin_memory()
+    v = flat[1:1 + c.numel()].view(c.shape)
+    v.copy_(c)
+    return v
+
+
+HOST_STEP_CASES = [("tiny", True, 0), ("tiny", False, 0), ("tiny", True, 1), ("fp8", True, 0),
+                   ("fp8", True, 1), ("fp8", False, 0)]
+
+
+@pytest.mark.parametrize("name,pinned,shift", HOST_STEP_CASES)
+def test_host_buffer_step_matches_device_step(name, pinned, shift):
+    """hpc_decode_step_host: pinned inputs are brought in by one copy kernel
+    through their device aliases (16-byte vectors, or bytes where an address
+    is not 16-byte aligned: shift moves the host lengths, block table and FP8
+    scales 4 bytes off), pageable ones by the copy engine; the output is
+    bit-identical to the device-buffer step."""
+    w = WORKLOADS[name]
     batch = make_batch(w, device="cuda")
-    dev_out, _ = run_step(batch, fused=False)
+    ctas = w.num_ctas or device_ctas(w.kv_dtype)
+    dev_out, _ = run_step(batch, num_ctas=ctas, fused=False)
     B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
-    h_q = batch.q.cpu().pin_memory()
-    h_sl = batch.seqlens.cpu().pin_memory()
-    h_bt = batch.block_table.cpu().pin_memory()
+    fp8 = w.kv_dtype == "e4m3"
+    h_q = _host_copy(batch.q, pinned, 0)
+    h_qs = _host_copy(batch.q_scale, pinned, shift) if fp8 else None
+    h_sl = _host_copy(batch.seqlens, pinned, shift)
+    h_bt = _host_copy(batch.block_table, pinned, shift)
+    assert h_q.is_pinned() == pinned and h_bt.is_pinned() == pinned
     h_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
     d_q, d_sl, d_bt = torch.empty_like(batch.q), torch.empty_like(batch.seqlens), \
         torch.empty_like(batch.block_table)
-    ws = hd.Workspace(B, Hq, Hkv, num_ctas=w.num_ctas)
-    hd.hpc_decode_step_host(h_q, None, h_sl, h_bt, h_out, d_q, None, d_sl, d_bt, ws.out,
-                            batch.k_cache, batch.v_cache, 1.0, 1.0, Hq, Hkv, w.sm_scale,
-                            w.num_ctas, w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse)
+    d_qs = torch.empty_like(batch.q_scale) if fp8 else None
+    ws = hd.Workspace(B, Hq, Hkv, num_ctas=ctas)
+    hd.hpc_decode_step_host(h_q, h_qs, h_sl, h_bt, h_out, d_q, d_qs, d_sl, d_bt, ws.out,
+                            batch.k_cache, batch.v_cache, batch.k_scale, batch.v_scale, Hq, Hkv,
+                            w.sm_scale, ctas, w.min_tiles, 0, ws.tmap, ws.part_o, ws.part_lse)
     torch.cuda.synchronize()
-    assert torch.equal(h_out, dev_out.cpu())
+    assert torch.equal(h_out.view(torch.int16), dev_out.cpu().view(torch.int16))
+    assert torch.equal(d_bt.cpu(), batch.block_table.cpu())
+    assert torch.equal(d_sl.cpu(), batch.seqlens.cpu())
+    if fp8:
+        assert torch.equal(d_qs.cpu(), batch.q_scale.cpu())
 
 
 def sample_rows(batch, n_random, seed, must_rows=()):
