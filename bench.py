@@ -549,7 +549,8 @@ def main():
         d2h = h_out.numel() * 2
         e2e = {"value": max(max_over_ranks(statistics.fmean(tot), world)), "unit": "us/step",
                "h2d_bytes_per_step": total, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "api": "hpc_decode_step_host_packed (one pinned input buffer copied in; the output stored by the attention grid into pinned host memory)",
+               "api": "hpc_decode_step_host_packed (one pinned input buffer read in by a copy kernel through its device alias; the output stored by the attention grid into pinned host memory)",
+               "gpu_launches_per_step": 3,  # copy-in, assign, attention (combine fused)
                "separate_buffers_us": statistics.fmean(sep),
                "separate_buffers_api": "hpc_decode_step_host (one copy kernel over the pinned input arrays; the output copied out by the copy engine)"}
 
