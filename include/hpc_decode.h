@@ -333,8 +333,9 @@ hpc_status hpc_decode_step(const void *d_q, const float *d_q_scale, const void *
  * aligned, bytes otherwise) and the assign kernel launches behind it as a
  * programmatic dependent; otherwise each array is one cudaMemcpyAsync
  * (synchronous for pageable memory).  The KV caches stay device-resident, as
- * they are in serving.  The host output is complete once `stream` has
- * finished.
+ * they are in serving.  Pinned inputs are read asynchronously: the caller
+ * rewrites them only after `stream` has passed the step.  The host output is
+ * complete once `stream` has finished.
  */
 hpc_status hpc_decode_step_host(const void *h_q, const float *h_q_scale, const int32_t *h_seqlens,
                                 const int32_t *h_block_table, void *h_out, void *d_q,
@@ -365,7 +366,8 @@ int64_t hpc_decode_packed_layout(int32_t B, int32_t Hq, int32_t max_pages_per_re
  * sections, and one device-to-host copy of d_out into h_out.  Pinned h_in
  * (with a 16-byte-aligned device alias) is read by a copy kernel through its
  * alias, one 16-byte load per thread, with the assign kernel launched as its
- * programmatic dependent; pageable h_in goes through the copy engine
+ * programmatic dependent (the caller rewrites h_in only after `stream` has
+ * passed the step); pageable h_in goes through the copy engine
  * (cudaMemcpyAsync, synchronous for pageable memory).  The same bytes move as
  * with the separate buffers, in one transfer each way.  With d_out NULL (and
  * d_unit_done given: the combine fused into the attention grid) the kernels
