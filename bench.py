@@ -2,8 +2,10 @@
 synthetic mixed-length batch on GB300, timed on the device.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-cpu-baseline] [--no-static]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-static] ...
 
+The headline workload defaults to `skewed` (B = 64, Hq = 64, Hkv = 8, BF16,
+60 short + 4 very long requests: the largest single-GPU configuration).
 Prints one JSON line (rank 0).  `value` is device-timed microseconds per
 step; `roofline` relates the attention kernel's algorithmic bytes per launch
 to its CUDA-event duration and the measured HBM copy peak; `e2e` is the same
@@ -14,9 +16,13 @@ static split-KV schedule on the same batch.  Side legs: the fused prologue
 (`rope_norm`), multi-query decode (`mtp`), the router GEMM sweep
 (`router_gemm`), extend / prefill attention on the vLLM comparison's
 shapes (`prefill`, TFLOP/s against the measured BF16 tensor peak) and that
-table's decode rows (`table4_decode`, with the best static split-KV).  Under
-torchrun every rank runs an independent replica (the path has no exchange
-step).
+table's decode rows (`table4_decode`, with the best static split-KV).  The
+line ends with two compact objects: `table3` (the six KV-length mixes of the
+vLLM post's Table 3, FP8, dynamic against the best static split) and
+`per_config` (every decode workload: step and attention time, attention
+bytes and fraction of the copy peak, best static split and the speed-up over
+it).  Under torchrun every rank runs an independent replica (the path has no
+exchange step).
 """
 
 from __future__ import annotations
@@ -133,23 +139,20 @@ def prefill_flops(seqlens, q_len, Hq):
 
 
 def profiled_traffic(kernel_src_hash, kv_dtype, workload):
-    """DRAM bytes per attention launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"attn_{kv_dtype.replace('e4m3', 'fp8')}_{workload}.md")
+    """DRAM bytes per attention launch from the committed ncu capture of this
+    workload (the JSON sidecar next to its summary under profiles/), if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_{kv_dtype.replace('e4m3', 'fp8')}_{workload}.json")
     try:
-        text = open(path).read()
-    except OSError:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256") != kernel_src_hash:
+    if d.get("kernel_source_sha256") != kernel_src_hash:
         return None
     try:
-        return float(vals["dram_bytes_per_launch_scaled"])
-    except (KeyError, ValueError):
+        return float(d["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -163,7 +166,7 @@ def kernel_source_hash():
 
 
 class ClockSampler:
-    """nvidia-smi samples (50 ms) with host timestamps, kept while running."""
+    """nvidia-smi samples (every 20 ms) with host timestamps, kept while running."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -175,7 +178,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
@@ -197,7 +200,11 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        return self.summary_over([(t0, t1)])
+
+    def summary_over(self, intervals):
+        """Samples whose host timestamp falls inside any of the intervals."""
+        inside = [p for t, p in self.samples if any(a <= t <= b for a, b in intervals)]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         def num(x):
@@ -268,7 +275,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="hy3_tp8")
+    ap.add_argument("--workload", default="skewed")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-static", action="store_true")
@@ -278,6 +285,10 @@ def parse_args():
     ap.add_argument("--no-router", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-table4-decode", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the compact per-workload summary at the end of the line")
+    ap.add_argument("--no-table3", action="store_true",
+                    help="skip the six Table-3 mixes (dynamic vs best static)")
     ap.add_argument("--prefill-shapes", default="",
                     help="comma-separated prefill/extend workloads (default: all of Table 4's)")
     ap.add_argument("--floor", type=int, default=None)
@@ -319,6 +330,15 @@ def max_over_ranks(x, world):
     return [float(o.item()) for o in out]
 
 
+def config_of(w, lens, floor, world):
+    """The workload's defining facts; both arms print this same dict."""
+    return {"workload": w.name, "description": w.description, "batch": w.batch,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 128,
+            "page": 64, "kv_dtype": w.kv_dtype, "live_tokens": int(sum(lens)), "floor": floor,
+            "l2": "GPU arm: L2 flushed before every step (256 MiB write outside the events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     """Reference arm: the fp64 oracle on the host cores, each step a bounded
     sample of the same workload, extrapolated by work."""
@@ -341,7 +361,8 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description},
+        "config": config_of(w, batch.seqlens.tolist(),
+                            w.min_tiles if args.floor is None else args.floor, world),
         "cpu_baseline": {"value": value, "unit": "us/step", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "us/step", "h2d_bytes_per_step": 0,
@@ -367,44 +388,11 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
-    kv_dtype = w.kv_dtype
-    fp8 = kv_dtype == "e4m3"
-    batch = make_batch(w, device=dev)
-    B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
-    floor = w.min_tiles if args.floor is None else args.floor
-    resident = hd.hpc_decode_num_ctas(local, hd.HPC_KV_FP8_E4M3 if fp8 else hd.HPC_KV_BF16)
-    ctas = args.ctas or resident * args.bins_per_cta  # bins of the plan
-    ws = hd.Workspace(B, Hq, Hkv, num_ctas=ctas, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     capture_stream = torch.cuda.Stream(device=dev)
-
-    def plan(tm, num_splits=0):
-        if num_splits:
-            hd.hpc_decode_plan_static(batch.seqlens, Hkv, batch.max_pages, num_splits, tm)
-        else:
-            hd.hpc_decode_plan(batch.seqlens, Hkv, batch.max_pages, ctas, floor, tm)
-
-    def attention(w_s, fused=True):
-        if fused:
-            hd.hpc_decode_attn_combine(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
-                                       batch.k_scale, batch.v_scale, batch.block_table,
-                                       batch.seqlens, Hq, Hkv, w.sm_scale, w_s.tmap, w_s.part_o,
-                                       w_s.part_lse, w_s.unit_done, w_s.out)
-        else:
-            hd.hpc_decode_attn(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
-                               batch.k_scale, batch.v_scale, batch.block_table, batch.seqlens,
-                               Hq, Hkv, w.sm_scale, w_s.tmap, w_s.part_o, w_s.part_lse)
-            hd.hpc_decode_combine(w_s.part_o, w_s.part_lse, w_s.tmap, B, Hq, Hkv, w_s.out)
-
-    def step(w_s, num_splits=0, fused=True):
-        """One decode step through the public step call: the assign kernel, then
-        the attention grid right behind it (fused combine unless fused=False)."""
-        hd.hpc_decode_step(batch.q, batch.q_scale, batch.k_cache, batch.v_cache, batch.k_scale,
-                           batch.v_scale, batch.block_table, batch.seqlens, Hq, Hkv, w.sm_scale,
-                           ctas, floor, num_splits, w_s.tmap, w_s.part_o, w_s.part_lse, w_s.out,
-                           unit_done=w_s.unit_done if fused else None)
+    sampler = ClockSampler(local)
+    timed_spans = []  # host (start, end) of every timed leg, for the clock record
 
     def graphed(fn):
         """fn captured once into a CUDA graph (the programmatic launch edges between
@@ -417,27 +405,123 @@ def main():
         torch.cuda.synchronize()
         return g.replay
 
-    def timed(n_steps, n_warm, run):
-        """Per-step device times (us) of run(), L2 flushed before each step; no
-        event sits between the kernels of a step, so programmatic launches overlap."""
+    def timed(n_steps, n_warm, run, before=None):
+        """Per-step device times (us) of run(), L2 flushed before each step
+        (and before() run, untimed, after the flush); no event sits between the
+        kernels of a step, so programmatic launches overlap."""
         for _ in range(n_warm):
             flush.fill_(1)
+            if before:
+                before()
             run()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_steps)]
+        t0 = time.time()
         for e0, e1 in evs:
             flush.fill_(1)
+            if before:
+                before()
             e0.record(stream)
             run()
             e1.record(stream)
         torch.cuda.synchronize()
+        timed_spans.append((t0, time.time()))
         return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+
+    class Rig:
+        """One decode workload on the device: its batch, a load-balanced
+        workspace, and the step / attention / static-schedule timings."""
+
+        def __init__(self, wl, floor=None, bins_per_cta=1, ctas=0):
+            self.w = wl
+            self.fp8 = wl.kv_dtype == "e4m3"
+            self.batch = make_batch(wl, device=dev)
+            self.B, self.Hq, self.Hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
+            self.floor = wl.min_tiles if floor is None else floor
+            self.resident = hd.hpc_decode_num_ctas(
+                local, hd.HPC_KV_FP8_E4M3 if self.fp8 else hd.HPC_KV_BF16)
+            self.ctas = ctas or wl.num_ctas or self.resident * bins_per_cta  # bins of the plan
+            self.ws = hd.Workspace(self.B, self.Hq, self.Hkv, num_ctas=self.ctas, device=dev)
+            self.lens = self.batch.seqlens.cpu().tolist()
+
+        def plan(self, tm, num_splits=0):
+            b = self.batch
+            if num_splits:
+                hd.hpc_decode_plan_static(b.seqlens, self.Hkv, b.max_pages, num_splits, tm)
+            else:
+                hd.hpc_decode_plan(b.seqlens, self.Hkv, b.max_pages, self.ctas, self.floor, tm)
+
+        def attention(self, w_s):
+            b = self.batch
+            hd.hpc_decode_attn_combine(b.q, b.q_scale, b.k_cache, b.v_cache, b.k_scale, b.v_scale,
+                                       b.block_table, b.seqlens, self.Hq, self.Hkv,
+                                       self.w.sm_scale, w_s.tmap, w_s.part_o, w_s.part_lse,
+                                       w_s.unit_done, w_s.out)
+
+        def step(self, w_s=None, num_splits=0, fused=True):
+            """One decode step through the public step call: the assign kernel, then
+            the attention grid right behind it (fused combine unless fused=False)."""
+            w_s = w_s or self.ws
+            b = self.batch
+            hd.hpc_decode_step(b.q, b.q_scale, b.k_cache, b.v_cache, b.k_scale, b.v_scale,
+                               b.block_table, b.seqlens, self.Hq, self.Hkv, self.w.sm_scale,
+                               self.ctas, self.floor, num_splits, w_s.tmap, w_s.part_o,
+                               w_s.part_lse, w_s.out, unit_done=w_s.unit_done if fused else None)
+
+        def attn_alone(self, n_steps, n_warm, w_s=None, num_splits=0):
+            """The dominant kernel alone, as every layer runs it on the step's map:
+            flush, rebuild the map (untimed, so it sits in L2 as in a model where all
+            layers share it), then time the attention launch by itself (a
+            standalone launch on a reused map waits for the kernel ahead of it)."""
+            w_s = w_s or self.ws
+            for _ in range(2):
+                self.step(w_s, num_splits)
+            return timed(n_steps, n_warm, lambda: self.attention(w_s),
+                         before=lambda: self.plan(w_s.tmap, num_splits))
+
+        def plan_facts(self, w_s=None):
+            w_s = w_s or self.ws
+            meta = hd.hpc_decode_read_meta(w_s.tmap)
+            if meta[3] != 0:
+                raise RuntimeError(f"{self.w.name}: device error flags {meta[3]}")
+            counts = w_s.tmap.chunk_count[:self.B * self.Hkv].tolist()
+            split_desc = sum(c for c in counts if c > 1)
+            nbytes = algorithmic_bytes(self.lens, self.Hq, self.Hkv, self.w.kv_dtype, meta[2],
+                                       split_desc)
+            return meta, nbytes
+
+        def static_sweep(self, n_steps, n_warm, with_attn=False):
+            """The in-house static split-KV schedule over S in {1, 2, 4, 8, 16, 32}
+            and the default S (smallest with B * Hkv * S >= the CTA count, capped
+            at the longest request's tiles); {S: (step us, attention us or None)}."""
+            max_n = max(max((L + 63) // 64 for L in self.lens), 1)
+            s_default = min(max(1, math.ceil(self.ctas / (self.B * self.Hkv))), max_n)
+            sweep = sorted({x for x in (1, 2, 4, 8, 16, 32, s_default) if x <= max_n})
+            res = {}
+            for S in sweep:
+                sws = hd.Workspace(self.B, self.Hq, self.Hkv, num_splits=S, device=dev)
+                tot = statistics.fmean(timed(n_steps, n_warm,
+                                             lambda sws=sws, S=S: self.step(sws, num_splits=S)))
+                att = (statistics.fmean(self.attn_alone(n_steps, n_warm, sws, S))
+                       if with_attn else None)
+                res[S] = (tot, att)
+                del sws
+            return res, s_default
+
+        def free(self):
+            del self.batch, self.ws
+
+    w = WORKLOADS[args.workload]
+    rig = Rig(w, args.floor, args.bins_per_cta, args.ctas)
+    batch, ws, kv_dtype, fp8 = rig.batch, rig.ws, w.kv_dtype, rig.fp8
+    B, Hq, Hkv, floor, ctas, resident = rig.B, rig.Hq, rig.Hkv, rig.floor, rig.ctas, rig.resident
+    lens = rig.lens
+    step = rig.step
 
     # ---- the timed region: K decode steps (assign + attention with fused combine),
     # launched directly (or replayed from a CUDA graph with --graph)
     run_step = graphed(lambda: step(ws)) if args.graph else (lambda: step(ws))
-    sampler = ClockSampler(local)
     for _ in range(args.warmup):
         flush.fill_(1)
         run_step()
@@ -455,43 +539,16 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
-    sampler.stop()
+    timed_spans.append((t0, t1))
     step_us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
-    meta = hd.hpc_decode_read_meta(ws.tmap)
-    if meta[3] != 0:
-        raise RuntimeError(f"device error flags {meta[3]}")
+    meta, nbytes = rig.plan_facts()
     num_desc = meta[2]
-    lens = batch.seqlens.cpu().tolist()
-    counts = ws.tmap.chunk_count[:B * Hkv].tolist()
-    split_desc = sum(c for c in counts if c > 1)
-    nbytes = algorithmic_bytes(lens, Hq, Hkv, kv_dtype, num_desc, split_desc)
     mean_step = statistics.fmean(step_us)
     all_steps = max_over_ranks(mean_step, world)
     value, agg_gbps = aggregate(all_steps, [nbytes["step"]] * world)
-    clocks = sampler.summary(t0, t1)
+    headline_clocks = sampler.summary(t0, t1)
 
-    # ---- the dominant kernel alone, as every layer runs it on the step's map:
-    # flush, rebuild the map (untimed, so it sits in L2 as in a model where all
-    # layers share it), then time the attention launch by itself (a standalone
-    # launch on a reused map, which reads nothing before the kernel ahead of
-    # it has finished)
-    def attn_alone(n_steps, n_warm, w_s, num_splits=0):
-        for _ in range(n_warm):
-            flush.fill_(1)
-            step(w_s, num_splits)
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n_steps)]
-        for e0, e1 in evs:
-            flush.fill_(1)
-            plan(w_s.tmap, num_splits)
-            e0.record(stream)
-            attention(w_s)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
-
-    attn_us_list = attn_alone(args.steps, args.warmup, ws)
+    attn_us_list = rig.attn_alone(args.steps, args.warmup)
     mean_attn = statistics.fmean(attn_us_list)
     peak, peak_kind = measured_peaks()
     achieved = nbytes["attn_fused"] / (mean_attn * 1e-6) / 1e9
@@ -557,17 +614,8 @@ def main():
     # ---- in-house static split-KV comparator on the same batch
     static = None
     if not args.no_static:
-        max_n = max(max((L + 63) // 64 for L in lens), 1)
-        s_default = min(max(1, math.ceil(ctas / (B * Hkv))), max_n)
-        sweep = sorted({s for s in (1, 2, 4, 8, 16, 32, s_default) if s <= max(max_n, 1)})
-        results = {}
-        for S in sweep:
-            sws = hd.Workspace(B, Hq, Hkv, num_splits=S, device=dev)
-            n_s = min(args.steps, 300)
-            tot = timed(n_s, 5, lambda sws=sws, S=S: step(sws, num_splits=S))
-            att = attn_alone(n_s, 5, sws, S)
-            results[S] = (statistics.fmean(tot), statistics.fmean(att))
-        best = min(results, key=lambda s: results[s][0])
+        results, s_default = rig.static_sweep(min(args.steps, 300), 5, with_attn=True)
+        best = min(results, key=lambda x: results[x][0])
         static = {"splits_default": s_default, "us_per_step_default": results[s_default][0],
                   "best_splits": best, "us_per_step_best": results[best][0],
                   "attn_us_best": results[best][1],
@@ -625,7 +673,7 @@ def main():
                                            batch.seqlens, Hq, Hkv, w.sm_scale, ws.tmap,
                                            ws.part_o, ws.part_lse, ws.unit_done, ws.out)
 
-            plan(ws.tmap)
+            rig.plan(ws.tmap)
             layer_us = statistics.fmean(timed(n_pro, args.warmup, layer))
             prologue["decode"] = {"workload": pw.name, "tokens": B, "us": dec_us,
                                   "bytes": prologue_bytes(B, Hq, Hkv, kv_dtype),
@@ -842,11 +890,57 @@ def main():
             del bd, wsd
         table4_decode = {"heads": "Hq=64, Hkv=8, head_dim 128, BF16", "shapes": rows}
 
+    # ---- every decode workload and the six Table-3 mixes, each in the
+    # headline's launch configuration: step, attention alone against the copy
+    # peak, and the best static split-KV step (compact, at the end of the line)
+    def decode_summary(r, step_mean=None, attn_mean=None, n=None):
+        n = n or min(max(args.steps, 20), 300)
+        if step_mean is None:
+            step_mean = statistics.fmean(timed(n, 3, r.step))
+        if attn_mean is None:
+            attn_mean = statistics.fmean(r.attn_alone(n, 3))
+        _, nb = r.plan_facts()
+        res, _ = r.static_sweep(n, 3)
+        S = min(res, key=lambda x: res[x][0])
+        return {"step_us": round(step_mean, 2), "attn_us": round(attn_mean, 2),
+                "attn_bytes": nb["attn_fused"],
+                "frac": round(nb["attn_fused"] / (attn_mean * 1e-6) / 1e9 / peak, 4),
+                "static_S": S, "static_us": round(res[S][0], 2),
+                "x_static": round(res[S][0] / step_mean, 3)}
+
+    per_config = None
+    if not args.no_per_config:
+        per_config = {}
+        for name in ("tiny", "hy3_tp8", "skewed", "uniform", "fp8"):
+            if name == w.name and args.bins_per_cta == 1 and not args.ctas and args.floor is None:
+                per_config[name] = decode_summary(rig, mean_step, mean_attn)
+                continue
+            r = Rig(WORKLOADS[name])
+            per_config[name] = decode_summary(r)
+            r.free()
+            del r
+    table3 = None
+    if not args.no_table3:
+        from load_balanced_paged_assign_gb300.workloads import TABLE3
+        table3 = {}
+        for name in TABLE3:
+            r = Rig(WORKLOADS[name])
+            d = decode_summary(r)
+            table3[name[3:]] = {k: d[k] for k in ("step_us", "frac", "static_S", "static_us",
+                                                  "x_static")}
+            r.free()
+            del r
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, desc = OracleTimer(batch).run(budget_s=12.0)
         cpu_baseline = {"value": us, "unit": "us/step", "cores": os.cpu_count(),
                         "kind": "oracle", "sample": desc}
+
+    sampler.stop()
+    clocks = sampler.summary_over(timed_spans)
+    clocks["span"] = "every timed leg of this run"
+    clocks["headline_samples"] = headline_clocks["samples"]
 
     if rank != 0:
         return
@@ -855,13 +949,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, "batch": B,
-                   "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128, "page": 64,
-                   "live_tokens": sum(lens), "persistent_ctas": min(ctas, resident),
-                   "bins": ctas, "floor": floor,
-                   "num_desc": num_desc, "budget": meta[1], "total_tiles": meta[0],
-                   "l2": "flushed before every step (256 MiB write outside the events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": config_of(w, lens, floor, world),
+        "plan": {"persistent_ctas": min(ctas, resident), "bins": ctas, "num_desc": num_desc,
+                 "budget": meta[1], "total_tiles": meta[0]},
         "gbps": agg_gbps, "pct_of_peak": agg_gbps / (peak * world),
         "attn_us": mean_attn, "unfused_us_per_step": unfused_us,
         "launch": "cuda graph replay per step" if args.graph else "direct launches", "bytes": nbytes,
@@ -880,6 +970,8 @@ def main():
         "table4_decode": table4_decode,
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
+        "table3": table3,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 

@@ -34,8 +34,9 @@
  *     OR-ed as HPC_FLAG_* bits into map->meta[3], which the caller reads after
  *     the stream completes (hpc_decode_read_meta does that for you).
  *   - Fixed geometry: head_dim = 128, page (= tile) size = 64 tokens,
- *     G = Hq / Hkv query heads per KV head with 1 <= G <= 8.  Query head hq
- *     uses KV head hq / G (contiguous groups).
+ *     G = Hq / Hkv query heads per KV head with 1 <= G <= 16.  Query head hq
+ *     uses KV head hq / G (contiguous groups); one descriptor serves the
+ *     whole group of its KV head ([vLLM] Compute and combine bullet).
  *   - Layouts are row-major:
  *       q         [B, Hq, 128]            bf16, or e4m3 for HPC_KV_FP8_E4M3
  *       q_scale   [B, Hq]                 fp32 (FP8 only): q = e4m3(q8) * q_scale
@@ -62,7 +63,7 @@ typedef void *hpc_stream_t; /* a cudaStream_t */
 typedef enum {
     HPC_OK = 0,
     HPC_ERR_ARG = -1,         /* null pointer, negative size, misaligned pointer, bad enum */
-    HPC_ERR_UNSUPPORTED = -2, /* head_dim != 128, G > 8, Hq % Hkv != 0, too large a batch */
+    HPC_ERR_UNSUPPORTED = -2, /* head_dim != 128, G > 16, Hq % Hkv != 0, too large a batch */
     HPC_ERR_WORKSPACE = -3,   /* task-map capacity below what the plan may write */
     HPC_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, tensor map) */
 } hpc_status;
@@ -77,7 +78,7 @@ typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
 
 #define HPC_HEAD_DIM 128
 #define HPC_PAGE_SIZE 64
-#define HPC_MAX_GROUP 8
+#define HPC_MAX_GROUP 16
 #define HPC_MAX_BATCH 16384
 #define HPC_MAX_QUERY_ROWS 16 /* multi-query decode: q_len * G query rows per KV head at most */
 
@@ -406,13 +407,17 @@ hpc_status hpc_decode_step_host_packed(const void *h_in, void *d_in, void *h_out
  *   d_meta_out  device int32[4] or NULL: receives the step's
  *               {total_tiles, budget, num_desc, error_flags}
  * Limits: the scratch must hold (num_ctas + B*Hkv) descriptors with their
- * partials, about 4.2 KB each at G = 8 (roughly 1,900 descriptors);
- * larger problems get HPC_ERR_WORKSPACE before anything is launched.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All
- * calls share the one array and leave their contents in it: calls that
- * overlap on the GPU (other streams, other host threads) race and must be
- * serialised by the caller.
+ * partials, G * 516 + 16 bytes each (about 4.2 KB at G = 8, roughly 1,900
+ * descriptors; 8.3 KB at G = 16, roughly 1,000); larger problems get
+ * HPC_ERR_WORKSPACE before anything is launched, and unsupported shapes the
+ * same status as hpc_decode_step.
+ * The first call in a CUDA context looks up the array's device address in
+ * that context (with its device current) and caches it under the context's
+ * id; make that first call before any stream capture.  A device reset or a
+ * different current context (cuCtxSetCurrent) makes the next call look the
+ * address up again.  All calls share the one array and leave their contents
+ * in it: calls that overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.
  */
 hpc_status hpc_decode_step_noalloc(const void *d_q, const float *d_q_scale, const void *d_k_cache,
                                    const void *d_v_cache, int32_t num_pages, float k_scale,

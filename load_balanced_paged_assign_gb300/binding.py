@@ -18,7 +18,7 @@ from . import _build
 HPC_OK, HPC_ERR_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_WORKSPACE, HPC_ERR_CUDA = 0, -1, -2, -3, -4
 HPC_KV_BF16, HPC_KV_FP8_E4M3 = 0, 1
 HPC_FLAG_BAD_SEQLEN, HPC_FLAG_DESC_OVERFLOW, HPC_FLAG_BAD_PAGE, HPC_FLAG_TIMEOUT = 1, 2, 4, 8
-HEAD_DIM, PAGE_SIZE, MAX_GROUP, MAX_QUERY_ROWS = 128, 64, 8, 16
+HEAD_DIM, PAGE_SIZE, MAX_GROUP, MAX_QUERY_ROWS = 128, 64, 16, 16
 HPC_ROPE_HALVES, HPC_ROPE_INTERLEAVED = 0, 1
 
 # Every symbol the header declares; the CPU tests check the library exports them all.

@@ -14,7 +14,6 @@ namespace hpc {
 
 constexpr int kHeadDim = 128;
 constexpr int kTile = 64;  // tokens per tile = tokens per page
-constexpr int kMaxGroup = 8;
 constexpr int kMaxRows = 16;  // query rows of one KV head in a descriptor: q_len * G
 constexpr int kConsumerWarps = 4;  // consumer warps per tile of a stage
 constexpr int kPlanThreads = 1024;

@@ -22,32 +22,77 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = HPC_NOALLOC_SCRATCH_BYTES;
+constexpr int64_t kScratchBytes = HPC_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+// The array's device address is a property of the CUDA context the library's
+// module is loaded in, not of the device ordinal: a cudaDeviceReset, or a
+// caller that makes another context current (cuCtxSetCurrent), loads the
+// module again at another address.  So the cached address is keyed by the
+// context's unique id (cuCtxGetId, never reused within a process) and looked
+// up again whenever the current context differs.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+struct ScratchEntry {
+    unsigned long long ctx_id;  // context the address belongs to
+    void *addr;                 // null: nothing cached
+};
+
 std::mutex g_mutex;
-void *g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
+ScratchEntry g_cache[kMaxDevices];  // per device, guarded by g_mutex
+std::once_flag g_fn_once;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// Unique id of the context current on this thread; false when there is none
+// or the driver does not provide the calls (then nothing is cached).
+bool current_context_id(unsigned long long *id) {
+    std::call_once(g_fn_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+    });
+    CUcontext ctx = nullptr;
+    if (!g_ctx_current || !g_ctx_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
 
-// Device address of the array on the current device.  Looked up once per
-// device with that device current; the symbol name itself is only a host
-// stand-in and must never be handed to a kernel.
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Device address of the array in the current context.  Looked up with
+// cudaGetSymbolAddress the first time a context calls (with that context's
+// device current); the symbol name itself is only a host stand-in and must
+// never be handed to a kernel.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+    ScratchEntry &c = g_cache[dev];
+    if (have_id && c.addr && c.ctx_id == id) {
+        *out = c.addr;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);  // makes the device's context current if none was
+    if (e != cudaSuccess) return e;
+    if (!have_id) have_id = current_context_id(&id);
+    c = have_id ? ScratchEntry{id, p} : ScratchEntry{0, nullptr};
+    *out = p;
     return cudaSuccess;
 }
 
@@ -59,18 +104,26 @@ extern "C" hpc_status hpc_decode_step_noalloc(
     const int32_t *d_block_table, int32_t max_pages_per_req, const int32_t *d_seqlens, int32_t B,
     int32_t Hq, int32_t Hkv, int32_t head_dim, float sm_scale, int32_t num_ctas,
     int32_t min_tiles_per_cta, void *d_out, int32_t *d_meta_out, hpc_stream_t stream) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || num_ctas < 1 || Hq % Hkv != 0) return HPC_ERR_ARG;
-    // Scratch layout: desc | bin_ptr | chunk_count | chunk_off | meta | part_o | part_lse.
+    // The shape checks of hpc_decode_step, first, so that an unsupported shape
+    // gets the same status there and here.
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages_per_req <= 0 || num_ctas < 1) return HPC_ERR_ARG;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_ARG;
+    if (head_dim != HPC_HEAD_DIM) return HPC_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0 || Hq / Hkv > HPC_MAX_GROUP) return HPC_ERR_UNSUPPORTED;
+    if (B > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
+    // Scratch layout: desc | bin_ptr | chunk_count | chunk_off | meta | part_o | part_lse,
+    // sized in 64-bit arithmetic (no term can wrap: num_ctas < 2^31, B * Hkv < 2^31,
+    // G <= 16) and checked against the array before anything is narrowed.
     const int64_t cap = hpc_decode_desc_capacity(B, Hkv, num_ctas);
     const int64_t units = (int64_t)B * Hkv > 0 ? (int64_t)B * Hkv : 1;
     const int64_t G = Hq / Hkv;
-    const size_t off_bins = align256((size_t)cap * 16);
-    const size_t off_count = off_bins + align256((size_t)(num_ctas + 1) * 4);
-    const size_t off_off = off_count + align256((size_t)units * 4);
-    const size_t off_meta = off_off + align256((size_t)units * 4);
-    const size_t off_part_o = off_meta + 256;
-    const size_t off_part_lse = off_part_o + align256((size_t)cap * G * HPC_HEAD_DIM * 4);
-    const size_t need = off_part_lse + align256((size_t)cap * G * 4);
+    const int64_t off_bins = align256(cap * 16);
+    const int64_t off_count = off_bins + align256(((int64_t)num_ctas + 1) * 4);
+    const int64_t off_off = off_count + align256(units * 4);
+    const int64_t off_meta = off_off + align256(units * 4);
+    const int64_t off_part_o = off_meta + 256;
+    const int64_t off_part_lse = off_part_o + align256(cap * G * HPC_HEAD_DIM * 4);
+    const int64_t need = off_part_lse + align256(cap * G * 4);
     if (cap < 0 || need > kScratchBytes) return HPC_ERR_WORKSPACE;  // too large for the array
 
     void *base = nullptr;
@@ -82,7 +135,7 @@ extern "C" hpc_status hpc_decode_step_noalloc(
     map.chunk_count = reinterpret_cast<int32_t *>(s + off_count);
     map.chunk_off = reinterpret_cast<int32_t *>(s + off_off);
     map.meta = reinterpret_cast<int32_t *>(s + off_meta);
-    map.cap_desc = (int32_t)cap;
+    map.cap_desc = (int32_t)cap;  // < 2^19: the layout fits the array
     map.cap_bins = num_ctas + 1;
     map.cap_units = (int32_t)units;
     map.B = map.Hkv = map.num_ctas = map.persistent = map.min_tiles = map.max_pages = 0;

@@ -102,7 +102,8 @@ def test_attn_argument_checks(hd):
     m.B, m.Hkv, m.num_ctas = 4, 1, 132
     E = hd.binding
     assert call_attn(hd, m, D=64) == E.HPC_ERR_UNSUPPORTED
-    assert call_attn(hd, m, Hq=12, Hkv=1) == E.HPC_ERR_UNSUPPORTED  # G = 12 > 8
+    assert call_attn(hd, m, Hq=17, Hkv=1) == E.HPC_ERR_UNSUPPORTED  # G = 17 > 16
+    assert call_attn(hd, m, Hq=64, Hkv=2) == E.HPC_ERR_UNSUPPORTED  # G = 32 > 16
     assert call_attn(hd, m, Hq=10, Hkv=4) == E.HPC_ERR_UNSUPPORTED  # Hq % Hkv != 0
     assert call_attn(hd, m, q=FAKE + 8) == E.HPC_ERR_ARG  # misaligned Q
     assert call_attn(hd, m, k=FAKE + 2) == E.HPC_ERR_ARG
@@ -302,3 +303,28 @@ def test_selftest_argument_checks(hd):
     assert L.hpc_selftest_wait_timeout(None, 1000, None) == E.HPC_ERR_ARG
     assert L.hpc_selftest_wait_timeout(FAKE, 0, None) == E.HPC_ERR_ARG
     assert L.hpc_selftest_wait_timeout(FAKE, 1000001, None) == E.HPC_ERR_ARG
+
+
+def test_noalloc_step_shape_checks_come_first(hd):
+    """The allocation-free step rejects what hpc_decode_step rejects, with the
+    same status and before it sizes or looks up its built-in scratch; only a
+    supported problem too large for the scratch gets HPC_ERR_WORKSPACE."""
+    L = hd.lib()
+    E = hd.binding
+
+    def call(B=4, Hq=8, Hkv=1, D=128, dtype=0, ctas=132, max_pages=4):
+        return L.hpc_decode_step_noalloc(FAKE, None, FAKE, FAKE, 10, 1.0, 1.0, dtype, FAKE,
+                                         max_pages, FAKE, B, Hq, Hkv, D, 0.088, ctas, 2, FAKE,
+                                         None, None)
+
+    assert call(D=64) == E.HPC_ERR_UNSUPPORTED
+    assert call(Hq=17, Hkv=1) == E.HPC_ERR_UNSUPPORTED  # G = 17 > 16
+    assert call(Hq=10, Hkv=4) == E.HPC_ERR_UNSUPPORTED
+    assert call(B=20000) == E.HPC_ERR_UNSUPPORTED  # above HPC_MAX_BATCH
+    assert call(dtype=7) == E.HPC_ERR_ARG
+    assert call(B=-1) == E.HPC_ERR_ARG
+    assert call(ctas=0) == E.HPC_ERR_ARG
+    assert call(max_pages=0) == E.HPC_ERR_ARG
+    # supported shapes whose descriptors and partials exceed the 8 MiB array
+    assert call(B=16384, Hq=16, Hkv=1) == E.HPC_ERR_WORKSPACE
+    assert call(ctas=2 ** 31 - 1) == E.HPC_ERR_WORKSPACE  # sized without wrapping

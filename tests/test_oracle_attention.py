@@ -80,7 +80,7 @@ def test_bf16_decoder_matches_torch():
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
-@pytest.mark.parametrize("hq,hkv", [(8, 1), (8, 2), (4, 4)])
+@pytest.mark.parametrize("hq,hkv", [(8, 1), (8, 2), (4, 4), (16, 1), (12, 1), (32, 2)])
 def test_matches_library_sdpa(kv_dtype, hq, hkv):
     lens = [1, 63, 64, 65, 128, 129, 300, 0]
     w = small_workload(len(lens), hq, hkv, kv_dtype)
