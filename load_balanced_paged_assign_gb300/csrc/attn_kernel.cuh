@@ -90,15 +90,10 @@ constexpr int kFlyMaxBatch = 1024;  // largest batch whose first descriptor is d
 constexpr int kWalkMaxBatch = 64;   // largest batch whose first bin is walked in-kernel
 constexpr int kWalkTiles = 8;       // tiles streamed on derived descriptors before the map is read
 
-// Warp-uniform bounded wait: lane 0 polls (so all lanes agree on the
-// outcome), then every lane re-observes the completed phase for its own
-// acquire of the data the phase guards.
+// Warp-uniform bounded wait: every lane polls the phase (so each lane
+// acquires the data the phase guards) and the lanes agree on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-    ok = __shfl_sync(kFullMask, ok, 0);
-    if (ok) mbar_try_wait(bar, parity);
-    return ok != 0;
+    return mbar_wait_warp(bar, parity, abort);
 }
 
 template <bool FP8, int STAGES, int TPS, int NB>
@@ -575,7 +570,8 @@ __device__ __forceinline__ void attn_producer(const CUtensorMap *tmap_k, const C
     }
     // Before leaving, make sure no copy this warp issued is still in flight
     // (bounded as well): the last phase issued on every stage must complete.
-    if (lane == 0) {
+    // Every lane waits, so none is parked at a warp barrier meanwhile.
+    {
         volatile int no_abort = 0;
         const uint32_t from = ps.it > (uint32_t)STAGES ? ps.it - STAGES : 0u;
         for (uint32_t j = from; j < ps.it; ++j)

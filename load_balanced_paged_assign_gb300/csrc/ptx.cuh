@@ -84,6 +84,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// The same wait for a whole warp, with every lane polling the barrier and a
+// warp-uniform result.  No lane is parked at a warp-synchronous instruction
+// (a shuffle or __syncwarp) while another lane polls: measured on GB300, a
+// warp whose lanes wait that way slows the shuffles and shared-memory traffic
+// of the SM's other warps several times over (a 24-shuffle chain took 3.3 us
+// instead of 0.5 us next to such warps).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort,
+                                               uint64_t limit_ns = 1000000000ull) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA / bulk
 // Tile load of a rank-4 / rank-5 tensor map into shared memory, completing
 // on `bar` with the tile's byte count.
