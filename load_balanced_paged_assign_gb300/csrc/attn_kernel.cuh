@@ -374,18 +374,22 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
         const int i = lane / p.G;
         qs = p.q_scale[((size_t)r * p.q_len + i) * p.Hq + h * p.G + (lane - i * p.G)];
     }
-    float qsg[Tr::kRows];
-#pragma unroll
-    for (int g = 0; g < Tr::kRows; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
     const int32_t *bt_row = p.block_table + (size_t)r * p.max_pages;
     const uint8_t *q_src = static_cast<const uint8_t *>(p.q) +
                            ((size_t)r * p.q_len * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
+    // the first 32 block-table entries are requested before the q-scales are
+    // broadcast, so the two loads share one round trip
+    int page0 = 0;
+    if (lane < min(32, te - tb)) page0 = bt_row[tb + lane];
+    float qsg[Tr::kRows];
+#pragma unroll
+    for (int g = 0; g < Tr::kRows; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
 
     for (int t0 = tb; t0 < te; t0 += 32) {  // 32 block-table entries at a time
         const int nt = min(32, te - t0);
         int page = 0;
         if (lane < nt) {
-            page = bt_row[t0 + lane];
+            page = t0 == tb ? page0 : bt_row[t0 + lane];
             if (page < 0 || page >= p.num_pages) {
                 ps.late_flags |= HPC_FLAG_BAD_PAGE;
                 page = 0;  // stay inside the cache; the result is flagged as invalid

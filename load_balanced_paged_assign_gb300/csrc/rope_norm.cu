@@ -410,15 +410,11 @@ __device__ __forceinline__ long long token_slot(const RopeNormArgs &a, int t, in
     return (long long)page * kTile + (pos % kTile);
 }
 
-// Bounded wait on an mbarrier phase, uniform across the warp: lane 0 polls,
-// the verdict is broadcast, then every lane observes the phase itself.
+// Bounded wait on an mbarrier phase, uniform across the warp: every lane
+// polls (and so observes the phase itself); the lanes agree on the outcome.
 __device__ __forceinline__ bool warp_wait_phase(uint64_t *bar, uint32_t parity,
                                                 volatile int *abort) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(bar, parity);
-    return ok != 0;
+    return mbar_wait_warp(bar, parity, abort);
 }
 
 template <bool FP8, int LAYOUT, bool NF>

@@ -109,33 +109,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool ok = true;
     int issued = 0;  // (producer lane) stages whose copies were issued
+    // The producer and MMA roles: the whole warp takes every (bounded) wait
+    // and lane 0 issues, so no lane is parked at a warp barrier while
+    // another polls (parked lanes slow the SM's other warps).
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t stream = policy_evict_first(), keep = policy_evict_last();
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % a.stages;
-                if (!mbar_wait(&empty[s], ((i / a.stages) & 1u) ^ 1u, abort)) {
-                    ok = false;
-                    break;
-                }
+        const uint64_t stream = policy_evict_first(), keep = policy_evict_last();
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % a.stages;
+            if (!mbar_wait_warp(&empty[s], ((i / a.stages) & 1u) ^ 1u, abort)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
                 uint8_t *st = smem + s * sb;
                 const int k = (kb0 + i) * kBK;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)sb);
                 tma_load_2d(st, &tx, &full[s], k, m0, stream);
                 tma_load_2d(st + kBM * kBK * 2, &thi, &full[s], k, n0, keep);
                 tma_load_2d(st + kBM * kBK * 2 + a.bn * kBK * 2, &tlo, &full[s], k, n0, keep);
-                ++issued;
             }
+            __syncwarp();
+            ++issued;
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kBM, a.bn);
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % a.stages;
-                if (!mbar_wait(&full[s], (i / a.stages) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
+        const uint32_t idesc = idesc_bf16_f32(kBM, a.bn);
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % a.stages;
+            if (!mbar_wait_warp(&full[s], (i / a.stages) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + s * sb);
                 const uint32_t sh = sa + kBM * kBK * 2, sl = sh + a.bn * kBK * 2;
@@ -148,10 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
             }
-            // every MMA issued has completed (also after a timeout: TMEM is
-            // only freed once this arrives)
-            umma_commit(tmem_full);
+            __syncwarp();
         }
+        // every MMA issued has completed (also after a timeout: TMEM is
+        // only freed once this arrives)
+        if (lane == 0) umma_commit(tmem_full);
     } else {
         // epilogue: TMEM lane quarter q = warp mod 4 holds rows 32 q .. 32 q + 31.
         // The ring is free once the last commit has arrived; each warp stages
@@ -161,11 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // N fall outside the tensor map and are not written.
         const int q = warp & 3;
         // (after an abort, copies may still land in the ring: nothing is staged)
-        int live = 1;
-        if (lane == 0) live = mbar_wait(tmem_full, 0, abort) && !*abort ? 1 : 0;
-        live = __shfl_sync(0xffffffffu, live, 0);
+        // every lane waits; the verdict is warp-uniform (the TMEM loads below are
+        // warp-collective)
+        const bool waited = mbar_wait_warp(tmem_full, 0, abort);
+        const bool live = __all_sync(0xffffffffu, waited && !*abort);
         if (live) {
-            mbar_try_wait(tmem_full, 0);  // every lane observes the completed phase
             tc_fence_after();
             const uint32_t row = tmem + ((uint32_t)(32 * q) << 16);
             const int chunks = a.bn / 32;
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         // no MMA may still write TMEM when it is freed (bounded, like every wait)
-        if (lane == 0) {
+        {
             volatile int no_abort = 0;
             mbar_wait(tmem_full, 0, &no_abort);
         }
