@@ -204,8 +204,9 @@ def test_deterministic_and_page_permutation_invariant(kv_dtype):
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("S", [1, 3, 8])
 @pytest.mark.parametrize("fused", [True, False])
-def test_static_schedule_parity(kv_dtype, S, fused):
-    w = small(len(BOUNDARY_LENS), 8, 2, kv_dtype)
+@pytest.mark.parametrize("hq", [16, 32])
+def test_static_schedule_parity(kv_dtype, S, fused, hq):
+    w = small(len(BOUNDARY_LENS), hq, 2, kv_dtype)
     batch = make_batch(w, device="cuda", seqlens=BOUNDARY_LENS, poison_tail=True, seed=11)
     out, ws = run_step(batch, num_splits=S, fused=fused)
     assert ws.tmap.to_host()["flags"] == 0

@@ -51,6 +51,19 @@ def test_two_calls_in_a_row_match_the_allocating_entry_point():
     check_against_step(second, 40, 1)
 
 
+def test_sixteen_head_groups_and_large_batches():
+    """Groups of 16 query heads per KV head (twice the partial rows per
+    descriptor) and a batch of 1500 requests (the CTAs wait for the task map
+    instead of deriving their first descriptor), both within the built-in
+    scratch."""
+    lens = [3000, 1, 64, 130, 20000, 0, 777]
+    w = Workload("na16", len(lens), 16, 1, seqlens=tuple(lens), seed=61)
+    check_against_step(make_batch(w, device="cuda", poison_tail=True), device_ctas("bf16"), 2)
+    lens = [int(x) for x in torch.randint(0, 300, (1500,), generator=torch.Generator().manual_seed(5))]
+    w = Workload("na1500", len(lens), 8, 1, seqlens=tuple(lens), kv_dtype="e4m3", seed=62)
+    check_against_step(make_batch(w, device="cuda", poison_tail=True), device_ctas("e4m3"), 2)
+
+
 def test_too_large_a_problem_is_rejected_before_launch():
     w = WORKLOADS["tiny"]
     batch = make_batch(w, device="cuda")
