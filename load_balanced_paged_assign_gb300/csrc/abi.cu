@@ -205,6 +205,7 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
         if (cap < 1) return HPC_ERR_CUDA;
         grid = std::min(grid, cap);
     }
+    const bool pulls_bins = map->persistent && map->num_ctas > grid;
     p.num_bins = map->num_ctas;
     p.bin_counter = map->meta + 4;
     p.min_tiles = map->min_tiles;
@@ -213,7 +214,13 @@ hpc_status launch_attention(const void *d_q, const float *d_q_scale, const void 
     // kernel: that kernel waited for everything before it, so the caller's
     // inputs are complete.  Behind any other kernel (a reused map) every read
     // waits.  The map must be load-balanced and planned for this block table.
-    p.fly = after_plan && map->persistent && map->max_pages == max_pages_per_req ? 1 : 0;
+    // Not with more bins than CTAs: a CTA pulls its next bin once it has read
+    // the map, and a derived first descriptor that spans the whole bin would
+    // delay that read to the bin's end, so the CTAs whose first bin is one
+    // descriptor would pull late and the others take more bins than their share.
+    p.fly = after_plan && map->persistent && map->max_pages == max_pages_per_req && !pulls_bins
+                ? 1
+                : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = fp8 ? launch_attn_fp8(nb, tk, tv, p, grid, s) : launch_attn_bf16(nb, tk, tv, p, grid, s);
     return cuda_status(e);
