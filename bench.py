@@ -268,6 +268,19 @@ class OracleTimer:
                 f"extrapolated by work; plus the assign oracle on the full batch")
         return us, desc
 
+    def single_thread(self, budget_s, seed=1):
+        """The same on one host thread, on a smaller sample: (us per step, rows)."""
+        np = self.np
+        order = np.random.default_rng(seed).permutation(self.rows_all)
+        per_work_1 = self.per_work * (os.cpu_count() or 1)  # rough single-thread cost
+        cum = np.cumsum(self.work[order])
+        n_rows = min(int(np.searchsorted(cum, budget_s / per_work_1)) + 1, len(order))
+        rows = np.sort(order[:n_rows])
+        t = time.perf_counter()
+        self.oracle.attention(rows=rows, num_threads=1, **self.cpu, **self.kw)
+        dt = time.perf_counter() - t
+        return dt * self.total_work / float(self.work[rows].sum()) * 1e6, int(n_rows)
+
 
 # ------------------------------------------------------------------ main
 def parse_args():
@@ -553,6 +566,13 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = nbytes["attn_fused"] / (mean_attn * 1e-6) / 1e9
     traffic = profiled_traffic(kernel_source_hash(), kv_dtype, w.name)
+
+    # ---- the same step replayed from a CUDA graph (host launch cost removed;
+    # each kernel's device-side launch remains), the second timing column
+    graph_us = None
+    if not args.graph:
+        graph_us = statistics.fmean(timed(min(args.steps, 1000), args.warmup,
+                                          graphed(lambda: step(ws))))
 
     # ---- the same step with the combine as its own kernel
     n_unf = min(args.steps, 1000)
@@ -933,9 +953,13 @@ def main():
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        us, desc = OracleTimer(batch).run(budget_s=12.0)
+        timer = OracleTimer(batch)
+        us, desc = timer.run(budget_s=12.0)
+        us1, rows1 = timer.single_thread(budget_s=3.0)
         cpu_baseline = {"value": us, "unit": "us/step", "cores": os.cpu_count(),
-                        "kind": "oracle", "sample": desc}
+                        "kind": "oracle", "sample": desc,
+                        "single_thread_us": us1,
+                        "single_thread_sample": f"{rows1} rows on 1 thread, extrapolated by work"}
 
     sampler.stop()
     clocks = sampler.summary_over(timed_spans)
@@ -954,7 +978,9 @@ def main():
                  "budget": meta[1], "total_tiles": meta[0]},
         "gbps": agg_gbps, "pct_of_peak": agg_gbps / (peak * world),
         "attn_us": mean_attn, "unfused_us_per_step": unfused_us,
-        "launch": "cuda graph replay per step" if args.graph else "direct launches", "bytes": nbytes,
+        "median_us_per_step": statistics.median(step_us),
+        "launch": "cuda graph replay per step" if args.graph else "direct launches",
+        "graph_us_per_step": graph_us, "bytes": nbytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "attn_kernel, fused combine (per-layer launch)",
