@@ -377,13 +377,17 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
     const int32_t *bt_row = p.block_table + (size_t)r * p.max_pages;
     const uint8_t *q_src = static_cast<const uint8_t *>(p.q) +
                            ((size_t)r * p.q_len * p.Hq + (size_t)h * p.G) * kHeadDim * Tr::kElem;
-    // the first 32 block-table entries are requested before the q-scales are
-    // broadcast, so the two loads share one round trip
+    // the first 32 block-table entries are requested with the q-scales, so
+    // the two loads share one round trip; the q-scales (FP8) are broadcast
+    // only after the first stage's copies are issued: the consumers need
+    // them once the stage has landed, so their load (from DRAM after a
+    // flush, where the block table is warm in L2) does not hold up the copies
     int page0 = 0;
     if (lane < min(32, te - tb)) page0 = bt_row[tb + lane];
     float qsg[Tr::kRows];
 #pragma unroll
-    for (int g = 0; g < Tr::kRows; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
+    for (int g = 0; g < Tr::kRows; ++g) qsg[g] = 1.f;
+    bool late_q = FP8;  // the q-scales are not broadcast yet
 
     for (int t0 = tb; t0 < te; t0 += 32) {  // 32 block-table entries at a time
         const int nt = min(32, te - t0);
@@ -433,10 +437,12 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                 si.desc_idx = idx;
                 si.count = count;
                 si.chunk_off = chunk_off;
+                if (!late_q) {
 #pragma unroll
-                for (int g = 0; g < Tr::kRows; ++g) si.qscale[g] = qsg[g];
+                    for (int g = 0; g < Tr::kRows; ++g) si.qscale[g] = qsg[g];
+                }
                 const uint32_t bytes = 2u * ns * Tr::kTileBytes + (first ? q_bytes : 0u);
-                if (defer) mbar_expect_tx(&full[stage], bytes);  // arrives below
+                if (defer || late_q) mbar_expect_tx(&full[stage], bytes);  // arrives below
                 else mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
                 for (int s = 0; s < TPS; ++s) {
@@ -460,6 +466,16 @@ __device__ __forceinline__ bool stream_desc(const CUtensorMap *tmap_k, const CUt
                     for (int i = 0; i < p.q_len; ++i)
                         bulk_load(smem + Tr::kOffQ + stage * Tr::kQBytes + i * q_group,
                                   q_src + i * q_token_stride, q_group, &full[stage]);
+            }
+            if (late_q) {
+#pragma unroll
+                for (int g = 0; g < Tr::kRows; ++g) qsg[g] = __shfl_sync(kFullMask, qs, g);
+                late_q = false;
+                if (lane == 0) {
+#pragma unroll
+                    for (int g = 0; g < Tr::kRows; ++g) info[stage].qscale[g] = qsg[g];
+                    if (!defer) mbar_arrive(&full[stage]);  // releases the q-scales with it
+                }
             }
             if (defer) {
                 wait_for_map(ps);
