@@ -3,7 +3,8 @@
 
 namespace hpc {
 
-// 4 stages x 1 tile x (16 KB K + 16 KB V) + Q: about 155 KB, one CTA per SM.
+// 4 stages x 1 tile x (16 KB K + 16 KB V), Q, two consumer -> combiner
+// hand-off slots and the combiner's staging: about 183 KB, one CTA per SM.
 #ifndef HPC_BF16_STAGES
 #define HPC_BF16_STAGES 4
 #endif
@@ -15,9 +16,9 @@ constexpr int kTpsBf16 = HPC_BF16_TPS;        // tiles per stage: 1 or 2
 using TraitsBf16 = AttnTraits<false, kStagesBf16, kTpsBf16, 1>;
 // Multi-query decode with 8 < q_len * G <= 16 query rows per KV head: twice
 // the state per consumer; one tile per stage (four consumers), four stages
-// and a single consumer -> combiner hand-off slot to fit.
+// and two hand-off slots still fit (about 227 KB).
 #ifndef HPC_BF16_STAGES_MQ
-#define HPC_BF16_STAGES_MQ 4  // with one hand-off slot (measured faster than 3 with two)
+#define HPC_BF16_STAGES_MQ 4
 #endif
 #ifndef HPC_BF16_TPS_MQ
 #define HPC_BF16_TPS_MQ 1

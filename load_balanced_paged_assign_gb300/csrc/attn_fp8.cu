@@ -3,8 +3,9 @@
 
 namespace hpc {
 
-// 4 stages x 2 tiles x (8 KB K + 8 KB V) + Q: about 150 KB, one CTA per SM; two
-// tiles per stage give 8 consumer warps, which FP8 needs to hide its per-tile latency.
+// 4 stages x 2 tiles x (8 KB K + 8 KB V), Q, two hand-off slots and the
+// combiner's staging: about 210 KB, one CTA per SM; two tiles per stage give
+// 8 consumer warps, which FP8 needs to hide its per-tile latency.
 #ifndef HPC_FP8_STAGES
 #define HPC_FP8_STAGES 4
 #endif
