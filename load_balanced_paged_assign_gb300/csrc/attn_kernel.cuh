@@ -1013,6 +1013,31 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
                         for (int e = 0; e < 4; ++e) s4[nb][e] += s4b[nb][e];
                 }
 
+                // FP8: the V^T fragments do not depend on P, so they are loaded
+                // and widened to f16 here and the conversions overlap the
+                // softmax's latencies (the two-row-block kernel, bound by its
+                // consumers, gains ~2%; it also no longer spills)
+                uint32_t va[8][4];
+                if (FP8) {
+                    // rows 2t4, 2t4+1, 2t4+8, 2t4+9 of the slice; dims 16g .. 16g+15
+                    uint4 Rv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 16 * sub + 2 * t4 + (q & 1) + (q >> 1) * 8;
+                        Rv[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
+                        if (tile * kTile + tok >= L) Rv[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    const uint32_t wA[4] = {Rv[0].x, Rv[0].y, Rv[0].z, Rv[0].w};
+                    const uint32_t wB[4] = {Rv[1].x, Rv[1].y, Rv[1].z, Rv[1].w};
+                    const uint32_t wC[4] = {Rv[2].x, Rv[2].y, Rv[2].z, Rv[2].w};
+                    const uint32_t wD[4] = {Rv[3].x, Rv[3].y, Rv[3].z, Rv[3].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
+                        e4m3x4_to_f16x2x2(__byte_perm(wA[j >> 1], wB[j >> 1], sel), va[j][0], va[j][1]);
+                        e4m3x4_to_f16x2x2(__byte_perm(wC[j >> 1], wD[j >> 1], sel), va[j][2], va[j][3]);
+                    }
+                }
                 // ---- online softmax (log2 domain); a token at or past a row's
                 // limit is masked for that row
                 const int tok0 = tile * kTile + 16 * sub;  // first token of this warp's slice
@@ -1081,30 +1106,11 @@ __device__ __forceinline__ bool attn_consumer(const AttnParams &p, uint8_t *smem
 
                 // ---- O^T += V^T . P^T (one V fragment feeds every row block)
                 if (FP8) {
-                    // rows 2t4, 2t4+1, 2t4+8, 2t4+9 of the slice; dims 16g .. 16g+15
-                    uint4 Rv[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int tok = 16 * sub + 2 * t4 + (q & 1) + (q >> 1) * 8;
-                        Rv[q] = lds128(sV + tok * 128 + ((g ^ (tok & 7)) << 4));
-                        if (tile * kTile + tok >= L) Rv[q] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    const uint32_t wA[4] = {Rv[0].x, Rv[0].y, Rv[0].z, Rv[0].w};
-                    const uint32_t wB[4] = {Rv[1].x, Rv[1].y, Rv[1].z, Rv[1].w};
-                    const uint32_t wC[4] = {Rv[2].x, Rv[2].y, Rv[2].z, Rv[2].w};
-                    const uint32_t wD[4] = {Rv[3].x, Rv[3].y, Rv[3].z, Rv[3].w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;
-                        const uint32_t x01 = __byte_perm(wA[j >> 1], wB[j >> 1], sel);
-                        const uint32_t x23 = __byte_perm(wC[j >> 1], wD[j >> 1], sel);
-                        uint32_t a0, a1, a2, a3;
-                        e4m3x4_to_f16x2x2(x01, a0, a1);
-                        e4m3x4_to_f16x2x2(x23, a2, a3);
+                    for (int j = 0; j < 8; ++j)
 #pragma unroll
                         for (int nb = 0; nb < NB; ++nb)
-                            mma_f16_16816(o[nb][j], a0, a1, a2, a3, b0[nb], b1[nb]);
-                    }
+                            mma_f16_16816(o[nb][j], va[j][0], va[j][1], va[j][2], va[j][3], b0[nb], b1[nb]);
                 } else {
                     const int tv = tok0 + 2 * t4;  // tokens of a0/a1 halves; +8 for a2/a3
                     const uint32_t mk01 =
