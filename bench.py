@@ -32,6 +32,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -156,12 +157,23 @@ def profiled_traffic(kernel_src_hash, kv_dtype, workload):
         return None
 
 
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(src):
+    """C/CUDA source without its comments, trailing blanks and empty lines
+    (string and character literals kept): what a capture's counters depend on."""
+    text = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash():
+    """sha256 of the attention kernel's code (comments and blank lines excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "load_balanced_paged_assign_gb300", "csrc")
     for name in ("attn_kernel.cuh", "attn_bf16.cu", "attn_fp8.cu", "ptx.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 

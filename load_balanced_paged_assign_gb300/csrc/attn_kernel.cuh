@@ -19,8 +19,8 @@
 //  * 4 * TPS consumer warps (warps 2 ..): warp w owns tokens 16 (w % 4) ..
 //    + 15 of tile w / 4 of every stage and keeps its own online-softmax
 //    state.  At a descriptor's end each consumer hands its state to a
-//    double-buffered shared-memory slot and goes straight on with the next
-//    stage; it never waits for the merge.
+//    shared-memory slot (double-buffered where the layout fits) and goes
+//    straight on with the next stage; it never waits for the merge.
 //  * warp 1 is a combiner: it merges the consumers' states of each finished
 //    descriptor, writes the BF16 output or the partial and its LSE, and counts
 //    the chunks of split units at once, so no consumer ever waits on that
