@@ -926,13 +926,13 @@ def main():
     # headline's launch configuration: step, attention alone against the copy
     # peak, and the best static split-KV step (compact, at the end of the line)
     def decode_summary(r, step_mean=None, attn_mean=None, n=None):
-        n = n or min(max(args.steps, 20), 300)
+        n = n or min(max(args.steps, 200), 300)  # at least 200 timed steps after 20 warm-ups
         if step_mean is None:
-            step_mean = statistics.fmean(timed(n, 3, r.step))
+            step_mean = statistics.fmean(timed(n, 20, r.step))
         if attn_mean is None:
-            attn_mean = statistics.fmean(r.attn_alone(n, 3))
+            attn_mean = statistics.fmean(r.attn_alone(n, 20))
         _, nb = r.plan_facts()
-        res, _ = r.static_sweep(n, 3)
+        res, _ = r.static_sweep(n, 20)
         S = min(res, key=lambda x: res[x][0])
         return {"step_us": round(step_mean, 2), "attn_us": round(attn_mean, 2),
                 "attn_bytes": nb["attn_fused"],
