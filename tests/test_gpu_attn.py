@@ -329,6 +329,25 @@ def test_large_batches_through_the_step(kv_dtype, B, hkv):
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("hq", [8, 16])
+def test_unit_split_over_many_bins(kv_dtype, hq):
+    """One 128K-token request beside two short ones, one KV head: the long
+    unit is cut into ~147 chunks (more than 64, so the merges take every LSE
+    round and every group of 32 chunks; with 16 query heads the two-row-block
+    merge), fused and separate combine, every row against the oracle."""
+    lens = [131072, 64, 3000]
+    w = Workload(f"longunit{hq}", len(lens), hq, 1, seqlens=tuple(lens), kv_dtype=kv_dtype,
+                 seed=5100 + hq)
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    ref = oracle_out(batch)
+    for fused in (True, False):
+        out, ws = run_step(batch, fused=fused)
+        assert_map_matches(ws, lens, 1, device_ctas(kv_dtype), w.min_tiles)
+        assert max(ws.tmap.chunk_count[:len(lens)].tolist()) > 64
+        assert_close(out, ref, kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("hq", [16, 12])
 @pytest.mark.parametrize("fused", [True, False])
 def test_group_of_up_to_sixteen_heads_full_size(kv_dtype, hq, fused):
