@@ -133,6 +133,36 @@ def test_dynamic_bins_parity_and_counter_reset(kv_dtype, bins_per_cta):
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_more_owed_merges_than_the_end_list_holds(kv_dtype):
+    """~54 one-tile bins per CTA over 4096 two-chunk units: a CTA completes
+    ~27 split units, more than its end-of-stream list holds (16), so the
+    combiner merges the rest at once.  Every row against the oracle, the
+    output run to run bit for bit, the counters back at zero."""
+    B, hkv = 2048, 2
+    lens = [128] * B
+    w = Workload("owed", B, 8 * hkv, hkv, seqlens=tuple(lens), kv_dtype=kv_dtype, seed=5200)
+    batch = make_batch(w, device="cuda", poison_tail=True)
+    bins = B * hkv * 2  # budget 1: every unit's two tiles land in two bins
+    ws = hd.Workspace(B, 8 * hkv, hkv, num_ctas=bins)
+    hd.hpc_decode_plan(batch.seqlens, hkv, batch.max_pages, bins, 1, ws.tmap)
+    ref = oracle_out(batch)
+    outs = []
+    for _ in range(2):
+        ws.out.fill_(float("nan"))
+        hd.hpc_decode_attn_combine(batch.q, batch.q_scale, batch.k_cache, batch.v_cache,
+                                   batch.k_scale, batch.v_scale, batch.block_table, batch.seqlens,
+                                   8 * hkv, hkv, w.sm_scale, ws.tmap, ws.part_o, ws.part_lse,
+                                   ws.unit_done, ws.out)
+        torch.cuda.synchronize()
+        meta = ws.tmap.meta.tolist()
+        assert meta[1] == 1 and meta[3] == 0 and meta[4] == 0
+        assert int(torch.count_nonzero(ws.unit_done)) == 0
+        outs.append(ws.out[:B].clone())
+    assert_close(outs[0], ref, kv_dtype)
+    assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("floor", [0, 1, 4, 1000])
 def test_floor_values(kv_dtype, floor):
     lens = [3000, 17, 64, 9000, 1]
